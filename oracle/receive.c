@@ -1,0 +1,152 @@
+/*
+ * Oracle: direct receive, packed rows -> grouped rowwise + columnwise-RHT
+ * NVFP4 operands with per-expert amax metadata.  TEST INFRASTRUCTURE ONLY
+ * (see oracle.h).
+ *
+ * TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR description:
+ * "the receiver builds the expert GEMM's NVFP4 GroupedTensor straight from the
+ * rows in one pass: the rowwise operand reuses the sender's codes and the
+ * columnwise RHT operand is quantized with a bound-derived per-expert scale,
+ * so no BF16 round trip or amax pass is needed."
+ * TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the dGLU
+ * epilogue", PR description: "the post-RHT columnwise amax is bounded by 4x
+ * the rowwise amax".
+ * TE PR #3324 "Enable NVFP4 row-scaled (per-token) backward for
+ * GroupedLinear", description: row-scaled (per-token) NVFP4 operands.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "oracle.h"
+
+static float get_f32(const uint8_t *p) { float v; memcpy(&v, p, 4); return v; }
+
+/* Per-expert metadata (readings R11, R17):
+ *   amax_row = max over the expert's rows of the trailer's A_t
+ *   amax_col = fl32(4 * amax_row)                      (the 4x bound)
+ *   S_enc    = min(fl32(2688 / amax_col), FLT_MAX) if amax_col > 0, else 1 */
+void or_expert_amax(const uint8_t *rows, int64_t H, const int32_t *offsets,
+                    int E, float *amax_row, float *amax_col, float *scale_enc)
+{
+    size_t S = or_row_bytes(H);
+    for (int e = 0; e < E; ++e) {
+        float a = 0.0f;
+        for (int32_t r = offsets[e]; r < offsets[e + 1]; ++r) {
+            float at = get_f32(rows + (size_t)r * S + S - 12);
+            if (at > a)
+                a = at;
+        }
+        float ac = 4.0f * a;
+        float se = 1.0f;
+        if (ac > 0.0f) {
+            se = 2688.0f / ac;
+            if (se > FLT_MAX)
+                se = FLT_MAX;
+        }
+        amax_row[e] = a;
+        amax_col[e] = ac;
+        scale_enc[e] = se;
+    }
+}
+
+/* Decoded value of element h of a packed row: sign * G[m] * s_b * S_t, exact
+ * (at most 6 significant bits, magnitude >= 2^-136) and therefore exact in
+ * float as well (reading R10). */
+static float decode(const uint8_t *row, int64_t H, size_t S, int64_t h)
+{
+    int code = (row[h / 2] >> ((h % 2) * 4)) & 0xf;
+    double sb = or_e4m3_value(row[H / 2 + h / 16]);
+    double St = (double)get_f32(row + S - 16);
+    return (float)(or_e2m1_value(code) * sb * St);
+}
+
+void or_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H,
+                             const int32_t *offsets, int E,
+                             const uint8_t *expert_mask,
+                             uint8_t *rw_codes, uint8_t *rw_scales,
+                             float *rw_row_scale, uint8_t *cw_codes,
+                             uint8_t *cw_scales, float *amax_row,
+                             float *amax_col, float *scale_enc,
+                             int rounding, uint64_t seed,
+                             uint16_t sign_mask, int64_t *report)
+{
+    size_t S = or_row_bytes(H);
+    (void)R_cap;
+    for (int i = 0; i < 4; ++i)
+        report[i] = 0;
+    or_expert_amax(rows, H, offsets, E, amax_row, amax_col, scale_enc);
+
+    for (int e = 0; e < E; ++e) {
+        if (expert_mask && !expert_mask[e])
+            continue;
+        int64_t off = offsets[e];
+        int64_t n = offsets[e + 1] - offsets[e];
+
+        /* rowwise operand (reading R8): the sender's codes and block scales,
+         * the token scale as the per-row FP32 scale */
+        for (int64_t r = off; r < off + n; ++r) {
+            const uint8_t *row = rows + (size_t)r * S;
+            memcpy(rw_codes + (size_t)r * (H / 2), row, (size_t)(H / 2));
+            memcpy(rw_scales + (size_t)r * (H / 16), row + H / 2, (size_t)(H / 16));
+            rw_row_scale[r] = get_f32(row + S - 16);
+        }
+
+        /* columnwise operand (readings R9-R13): per hidden column h and per
+         * block of 16 consecutive rows of this expert, RHT along the rows,
+         * then an E4M3 block scale from the bound-derived per-expert scale
+         * and E2M1 codes.  Layout: expert e's codes are [H][n/2] bytes at
+         * byte off*H/2, its scales [H][n/16] at byte off*H/16. */
+        float se = scale_enc[e];
+        float ce = se / 6.0f;
+        float bound = 4.0f * amax_row[e];
+        uint8_t *cc = cw_codes + (size_t)off * (size_t)(H / 2);
+        uint8_t *cs = cw_scales + (size_t)off * (size_t)(H / 16);
+        for (int64_t h = 0; h < H; ++h) {
+            for (int64_t j = 0; j < n / 16; ++j) {
+                float d[16], y[16];
+                float dmax = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    d[i] = decode(rows + (size_t)(off + 16 * j + i) * S, H, S, h);
+                    dmax = fmaxf(dmax, fabsf(d[i]));
+                }
+                or_rht16_f32(d, sign_mask, y);
+                float bmax = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    float ay = fabsf(y[i]);
+                    bmax = fmaxf(bmax, ay);
+                    if (ay > bound)
+                        report[1] += 1;
+                    if (ay > 4.0f * dmax)
+                        report[3] += 1;
+                }
+                float sprod = bmax * ce;
+                int s = or_e4m3_rne_sat((double)sprod);
+                if ((double)sprod > 448.0)
+                    report[0] += 1;
+                float sval = (float)or_e4m3_value(s);
+                float r = (sval == 0.0f) ? 0.0f : se / sval;
+                cs[h * (n / 16) + j] = (uint8_t)s;
+                for (int i = 0; i < 16; ++i) {
+                    float v = fabsf(y[i]) * r;
+                    if (v > 6.0f)
+                        report[2] += 1;
+                    double sv = signbit(y[i]) ? -(double)v : (double)v;
+                    int64_t pos = 16 * j + i; /* row within the expert */
+                    int code;
+                    if (rounding == 1)
+                        code = or_e2m1_sr(sv, or_sr_byte(seed, 1u,
+                                   (uint64_t)off * (uint64_t)H + (uint64_t)h * (uint64_t)n + (uint64_t)pos));
+                    else
+                        code = or_e2m1_rne(sv);
+                    size_t byte = (size_t)h * (size_t)(n / 2) + (size_t)(pos / 2);
+                    if (pos % 2 == 0)
+                        cc[byte] = (uint8_t)((cc[byte] & 0xf0) | code);
+                    else
+                        cc[byte] = (uint8_t)((cc[byte] & 0x0f) | (code << 4));
+                }
+            }
+        }
+    }
+}
