@@ -1,0 +1,421 @@
+"""Benchmark of the NVFP4 EP hot path: route plan + NVFP4 pack + direct receive.
+
+Workload: 4096 tokens x 4096 hidden BF16 ~N(0,1) with 0.1% of entries x50;
+16 experts, softmax-of-Gaussian top-2 routing with 2 experts forced empty;
+alignment 128; round-to-nearest-even (the dispatch-forward configuration).
+A step is one pass of the whole path over one batch: route plan (2 kernels),
+NVFP4 pack with the routing gather (1 kernel), direct receive (per-expert
+amax + tiled rowwise / columnwise-RHT kernel).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank processes its own
+batch (replicas: the path shards by token batch with no exchange on one
+GPU), ``value`` is the sum over ranks of tokens / the slowest rank's time.
+The reference arm (``--impl reference``) times the plain CPU oracle on the
+host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 pack+direct-receive tokens/s and achieved HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+WORKLOAD_CFG = 2          # the dispatch-forward config the metric is quoted on
+N_SETS = 6                # rotating buffer sets: ~560 MB touched per rotation > 129 MB L2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
+    region (read-only queries)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.gpu = gpu_index
+        self.enabled = enabled
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        if not self.enabled:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [t.strip() for t in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    mhz.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        finally:
+            os.unlink(self.path)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(mhz)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+DR_SOURCES = ["nvfp4_quantization_gb300/csrc/receive.cu", "nvfp4_quantization_gb300/csrc/epq_device.cuh"]
+
+
+def profiled_traffic(kernel: str, sources) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d[kernel]
+        if rec.get("source_sha") != source_sha(sources):
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def algorithmic_bytes(T, H, k, E, R, S):
+    """Bytes the method must move (padding rows count: they are real rows)."""
+    route = 4 * T * k * 2 + 4 * (2 * E + 1)          # ids in, dest out, offsets / counts
+    pack = 2 * T * H + 4 * T * k + R * S             # tokens + dest in, rows out
+    dr = R * S + R * (9 * H // 16 + 4) + R * (9 * H // 16) + 12 * E
+    return route, pack, dr
+
+
+class BufferSet:
+    """One set of device buffers and the CUDA graphs of one step on them."""
+
+    def __init__(self, torch, nq, w, tok_host, topk_host):
+        self.tok = tok_host.cuda()
+        self.topk = topk_host.cuda()
+        self.plan = nq.ep_route_plan(self.topk, w.E, w.A)
+        ws_b = int(nq.lib().ep_route_workspace_bytes(w.T, w.k, w.E))
+        self.ws = torch.empty((ws_b + 3) // 4, dtype=torch.int32, device="cuda")
+        self.rows = torch.empty((self.plan.R_cap, nq.row_bytes(w.H)), dtype=torch.uint8, device="cuda")
+        self.out = nq.alloc_grouped(self.plan.R_cap, w.H, w.E, "cuda")
+        self.w, self.nq = w, nq
+        self.route_pack()
+        self.receive()
+
+    def route_pack(self):
+        w, nq = self.w, self.nq
+        nq.ep_route_plan(self.topk, w.E, w.A, R_cap=self.plan.R_cap, plan=self.plan, workspace=self.ws)
+        nq.ep_nvfp4_pack(self.tok, self.plan, rows=self.rows, rounding=w.rounding, seed=w.seed)
+
+    def receive(self):
+        w, nq = self.w, self.nq
+        nq.ep_nvfp4_direct_receive(self.rows, w.H, self.plan.offsets, w.E, out=self.out, rounding=w.rounding,
+                                   seed=w.seed, sign_mask=w.sign_mask, status=self.plan.status)
+
+    def capture(self, torch):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        self.gA, self.gB = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.gA, stream=s):
+                self.route_pack()
+            with torch.cuda.graph(self.gB, stream=s):
+                self.receive()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+
+
+def gpu_arm(args, rank, world, local):
+    import torch
+
+    import nvfp4_quantization_gb300 as nq
+    import workloads
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier(device_ids=[local])
+
+    w = workloads.make(WORKLOAD_CFG, seed=2 + 1000 * rank)
+    T, H, k, E = w.T, w.H, w.k, w.E
+    tok_host = torch.from_numpy(w.tokens.view(np.int16)).view(torch.bfloat16)
+    topk_host = torch.from_numpy(np.ascontiguousarray(w.topk))
+    sets = [BufferSet(torch, nq, w, tok_host, topk_host) for _ in range(N_SETS)]
+    torch.cuda.synchronize()
+    st = int(sets[0].plan.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} after the first pass")
+    R = int(sets[0].plan.offsets[-1].item())
+    S = nq.row_bytes(H)
+    for b in sets:
+        b.capture(torch)
+
+    # ---- timed region: K steps, rotating buffer sets (cold L2 per step)
+    K, W = args.steps, args.warmup
+    every = max(1, K // 2000)
+    for i in range(W):
+        b = sets[i % N_SETS]
+        b.gA.replay()
+        b.gB.replay()
+    torch.cuda.synchronize()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range((K + every - 1) // every)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    clocks.start()
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    t0.record()
+    for i in range(K):
+        b = sets[i % N_SETS]
+        if i % every == 0:
+            e = ev[i // every]
+            e[0].record()
+            b.gA.replay()
+            e[1].record()
+            b.gB.replay()
+            e[2].record()
+        else:
+            b.gA.replay()
+            b.gB.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    clk = clocks.stop()
+    barrier()
+    ms_total = t0.elapsed_time(t1)
+    if dist is not None:
+        tt = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / K
+    ms_a = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    ms_b = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    st = int(sets[0].plan.status.item())
+    route_b, pack_b, dr_b = algorithmic_bytes(T, H, k, E, R, S)
+    res = dict(T=T, H=H, k=k, E=E, R=R, S=S, ms_step=ms_step, ms_a=ms_a, ms_b=ms_b, wall_s=wall1 - wall0,
+               clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), world=world, w=w)
+
+    # ---- end to end through the public API with host buffers
+    res["e2e"] = e2e_measure(torch, nq, w, sets[0], tok_host, topk_host, R, args.e2e_steps)
+    return res
+
+
+def e2e_measure(torch, nq, w, b, tok_host, topk_host, R, steps):
+    """Each step: pinned host tokens + routing -> device, the three public
+    calls (eager), grouped operands + metadata -> pinned host."""
+    H, E = w.H, w.E
+    tok_pin = tok_host.pin_memory()
+    topk_pin = topk_host.pin_memory()
+    srcs = [b.out["rw_codes"][:R], b.out["rw_scales"][:R], b.out["rw_row_scale"][:R],
+            b.out["cw_codes"][: R * H // 2], b.out["cw_scales"][: R * H // 16],
+            b.out["amax_row"], b.out["amax_col"], b.out["cw_scale_enc"]]
+    dsts = [torch.empty(s.shape, dtype=s.dtype, pin_memory=True) for s in srcs]
+    h2d = tok_pin.numel() * 2 + topk_pin.numel() * 4
+    d2h = sum(s.numel() * s.element_size() for s in srcs)
+
+    def step():
+        b.tok.copy_(tok_pin, non_blocking=True)
+        b.topk.copy_(topk_pin, non_blocking=True)
+        b.route_pack()
+        b.receive()
+        for s, d in zip(srcs, dsts):
+            d.copy_(s, non_blocking=True)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ok = torch.equal(dsts[3][: 1 << 16].cuda(), srcs[3][: 1 << 16])
+    return dict(ms=ms, h2d=h2d, d2h=d2h, ok=bool(ok))
+
+
+def oracle_pass(o, w, tokens, topk):
+    """Route plan + NVFP4 pack + direct receive of one batch on the oracle."""
+    off, cnt, dest, _ = o.route_plan(topk, w.E, w.A)
+    R_cap = o.rows_capacity(tokens.shape[0], w.k, w.E, w.A)
+    rows = o.nvfp4_pack(tokens, dest, w.k, off, cnt, w.E, R_cap, rounding=w.rounding, seed=w.seed)
+    o.nvfp4_direct_receive(rows, w.H, off, w.E, rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask)
+
+
+def cpu_baseline(w) -> dict:
+    """The oracle, as it stands (single-threaded C), on the whole batch once."""
+    import oracle as o
+    o.build()
+    t0 = time.perf_counter()
+    oracle_pass(o, w, w.tokens, w.topk)
+    dt = time.perf_counter() - t0
+    return {"value": w.T / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one pass over the full batch ({w.T} tokens), single-threaded C oracle, {dt:.2f} s"}
+
+
+def reference_arm(args, rank, world):
+    """--impl reference: the oracle on the host cores, each step a slice of
+    the same workload sized so that warm-up + K steps take about two minutes."""
+    if rank != 0:
+        return None
+    import oracle as o
+    import workloads
+    o.build()
+    w = workloads.make(WORKLOAD_CFG)
+    t0 = time.perf_counter()
+    oracle_pass(o, w, w.tokens[:512], w.topk[:512])
+    per_tok = (time.perf_counter() - t0) / 512
+    K, W = args.steps, args.warmup
+    n = int(max(1, min(w.T, 120.0 / max(K + W, 1) / per_tok)))
+
+    def run(i):
+        a = (i * n) % w.T
+        idx = np.arange(a, a + n) % w.T
+        oracle_pass(o, w, np.ascontiguousarray(w.tokens[idx]), np.ascontiguousarray(w.topk[idx]))
+
+    for i in range(W):
+        run(i)
+    t0 = time.perf_counter()
+    for i in range(K):
+        run(W + i)
+    dt = time.perf_counter() - t0
+    value = n * K / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": dt * 1e3 / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.description, "tokens_per_step": n},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{n} consecutive tokens of the batch (and their routing) per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    r = gpu_arm(args, rank, world, local)
+    if rank != 0:
+        return
+    peak, peak_kind = load_peaks()
+    route_b, pack_b, dr_b = r["bytes"]
+    w = r["w"]
+    tokens_s = world * r["T"] / (r["ms_step"] * 1e-3)
+    dr_gbs = dr_b / (r["ms_b"] * 1e-3) / 1e9
+    pack_gbs = (route_b + pack_b) / (r["ms_a"] * 1e-3) / 1e9
+    path_gbs = (route_b + pack_b + dr_b) / (r["ms_step"] * 1e-3) / 1e9
+    e2e = r["e2e"]
+    line = {
+        "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.description, "T": r["T"], "H": r["H"], "E": r["E"], "k": r["k"], "A": w.A,
+                   "R": r["R"], "rounding": "rne", "l2": f"{N_SETS} rotating buffer sets (inputs+outputs "
+                   f"> 4x L2), back-to-back CUDA-graph steps", "parallelism": f"replicas x{world}"},
+        "path": {"gbs": path_gbs, "frac_of_peak": path_gbs / peak, "bytes_per_step": route_b + pack_b + dr_b,
+                 "route_pack_ms": r["ms_a"], "route_pack_gbs": pack_gbs, "direct_receive_ms": r["ms_b"],
+                 "direct_receive_gbs": dr_gbs},
+        "roofline": {"kernel": "ep_nvfp4_direct_receive (expert amax + tiled transform)", "bound": "hbm",
+                     "achieved": dr_gbs, "peak": peak, "unit": "GB/s", "frac": dr_gbs / peak,
+                     "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": dr_b,
+                     "traffic": profiled_traffic("direct_receive", DR_SOURCES)},
+        "e2e": {"value": world * r["T"] / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"],
+                "api": "eager ep_route_plan / ep_nvfp4_pack / ep_nvfp4_direct_receive", "checked": e2e["ok"]},
+        "gpu_launches": 5 * args.steps,
+        "clocks": r["clocks"],
+        "device_status": r["status"],
+        "timed_wall_s": r["wall_s"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

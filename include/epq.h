@@ -1,0 +1,223 @@
+/*
+ * epq.h -- C ABI of libepq.so: NVFP4 / MXFP8 expert-parallel token
+ * quantisation on one GB300 (sm_103a).
+ *
+ * The method is the one described by four TransformerEngine pull-request
+ * pages, cited below by title and section:
+ *   TE PR #3753 "[Common][PyTorch] Add NVFP4 EP dispatch and combine backward"
+ *   TE PR #3270 "[Common][PyTorch] EP dispatch with unfused MXFP8 quantization"
+ *   TE PR #3324 "[PyTorch] Enable NVFP4 row-scaled (per-token) backward for
+ *               GroupedLinear"
+ *   TE PR #3755 "[PyTorch] Optionally derive FC1 dy NVFP4 amaxes from the dGLU
+ *               epilogue"
+ * The cross-GPU expert-parallel transport of those pages is replaced, on one
+ * GPU, by a local routing plan that places every (token, expert) pair in an
+ * expert-contiguous, alignment-padded row order.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers named "device" are CUDA device memory owned by the caller; the
+ *   library never allocates, frees or synchronises, and never keeps a pointer
+ *   after the call returns.  Every call only enqueues work on `stream` (a
+ *   cudaStream_t passed as void*; NULL = the legacy default stream), so every
+ *   call can be captured in a CUDA graph.
+ * - Device guard: the call makes the device that owns the first input pointer
+ *   current for its duration (and restores the previous device); every other
+ *   pointer must live on that same device, else EP_ERR_DEVICE (TE PR #3753,
+ *   commit "guard the NVFP4 EP bindings with the input tensor's device").
+ * - Errors found on the host (null pointer, bad size, bad argument, too small
+ *   a buffer, pointer on the wrong device) return a negative ep_status before
+ *   anything is enqueued.  A failed launch returns EP_ERR_CUDA.  Errors that
+ *   only the data can reveal (a bad routing id, a wait that gave up) are ORed
+ *   into the caller's device word *dev_status as EP_DEV_ERR_* bits and the
+ *   offending item is skipped; kernels never trap.  The caller reads
+ *   dev_status after its own synchronisation.
+ * - Outputs are bit-deterministic for a given input, routing, seed and sign
+ *   mask.  Rows in [R, R_cap) of every row-indexed output are left untouched,
+ *   R = expert_offsets[E].
+ * - Shapes: T tokens, H hidden (H % 32 == 0), k routing slots per token
+ *   (1 <= k <= 32), E experts (1 <= E <= 1024), A per-expert alignment
+ *   (A > 0, A % 128 == 0), R_cap rows of capacity (< 2^31).
+ */
+#ifndef EPQ_H
+#define EPQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_NULL = -1,      /* a required pointer is NULL                    */
+    EP_ERR_SHAPE = -2,     /* T, H, k, E out of range or H % 32 != 0        */
+    EP_ERR_ALIGN = -3,     /* A not a positive multiple of 128, or a
+                              pointer not 16-byte aligned                   */
+    EP_ERR_CAPACITY = -4,  /* R_cap or a workspace too small                */
+    EP_ERR_ARG = -5,       /* bad rounding mode or other argument           */
+    EP_ERR_DEVICE = -6,    /* pointer not device memory of the input device */
+    EP_ERR_CUDA = -7       /* a CUDA call failed                            */
+} ep_status;
+
+enum { EP_ROUND_RNE = 0, EP_ROUND_SR = 1 };
+
+/* Bits ORed into *dev_status by the kernels. */
+enum {
+    EP_DEV_ERR_BAD_EXPERT = 1u,  /* routing id outside [-1, E): slot dropped  */
+    EP_DEV_ERR_DUP_EXPERT = 2u,  /* id repeated within a token: later dropped */
+    EP_DEV_ERR_TIMEOUT = 4u,     /* a bounded wait gave up; outputs invalid   */
+    EP_DEV_ERR_CAPACITY = 8u     /* expert_offsets[E] > R_cap: rows skipped   */
+};
+
+/* Bytes of one packed NVFP4 row: roundup16(9H/16 + 16). */
+size_t ep_nvfp4_row_bytes(int64_t H);
+
+/* Upper bound on R = sum_e ceil(c_e / A) * A over any routing: T*k + E*(A-1). */
+int64_t ep_rows_capacity(int64_t T, int k, int E, int A);
+
+/* Device workspace needed by ep_route_plan (ceil(T/1024) * E * 4 bytes, at
+ * least 16). */
+size_t ep_route_workspace_bytes(int64_t T, int k, int E);
+
+/*
+ * ep_route_plan -- expert-contiguous placement of every (token, slot).
+ * TE PR #3270, description and sequence diagram: dispatch returns the received
+ * rows "expert-major" as a per-expert grouped tensor; review thread: each
+ * expert slot is aligned to a multiple of 128 rows for the grouped packed
+ * scales; TE PR #3753, commit "layer_args": the backward takes (top_k,
+ * alignment, topk_idx_dtype).
+ *   topk_idx        device int32 [T, k], row-major; -1 = dropped slot.  An id
+ *                   >= E or < -1 sets EP_DEV_ERR_BAD_EXPERT and is dropped; an
+ *                   id repeated within a token sets EP_DEV_ERR_DUP_EXPERT and
+ *                   the later slot is dropped.
+ *   expert_offsets  device int32 [E+1] out: expert e owns rows
+ *                   [offsets[e], offsets[e+1]); offsets[E] = R.
+ *   expert_counts   device int32 [E] out: c_e, tokens routed to e.  The
+ *                   n_e - c_e trailing rows of expert e are padding rows.
+ *   dest            device int32 [T*k] out: row of (t, j), or -1 if dropped.
+ *                   Within an expert, rows follow ascending token order.
+ *   workspace       device, ws_bytes >= ep_route_workspace_bytes(T, k, E).
+ *   R_cap           capacity the rows buffers will have; must be at least
+ *                   ep_rows_capacity(T, k, E, A) (EP_ERR_CAPACITY otherwise).
+ * Two kernels; T = 0 is allowed (all offsets and counts 0).
+ */
+ep_status ep_route_plan(const int32_t *topk_idx, int64_t T, int k, int E, int A,
+                        int64_t R_cap, int32_t *expert_offsets,
+                        int32_t *expert_counts, int32_t *dest, void *workspace,
+                        size_t ws_bytes, uint32_t *dev_status, void *stream);
+
+/*
+ * ep_nvfp4_pack -- quantise each BF16 token once into a packed NVFP4 row and
+ * write that row to each of its destinations; fill padding rows.
+ * TE PR #3753, PR description and the review thread on the EP header comment:
+ * "the sender packs each token into one NVFP4 row (E2M1 codes, E4M3 block
+ * scales and a power-of-two FP32 token scale)"; the combine backward "uses
+ * stochastic rounding per the recipe".
+ *   tokens_bf16     device bf16 [T, H] row-major, finite values.
+ *   dest, expert_offsets, expert_counts: as produced by ep_route_plan.
+ *   rows            device u8 [R_cap, S], S = ep_nvfp4_row_bytes(H), 16-byte
+ *                   aligned.  Row layout: [0, H/2) E2M1 codes (element 2i in
+ *                   the low nibble of byte i); [H/2, 9H/16) E4M3 block scales,
+ *                   one per 16 elements; zeros up to S-16; trailer at S-16 =
+ *                   {f32 token scale S_t = 2^k, f32 token amax A_t,
+ *                   u32 source token id, u32 0}.  A padding row is the packing
+ *                   of an all-zero token with id 0xFFFFFFFF.
+ *   rounding        EP_ROUND_RNE or EP_ROUND_SR (element codes only; scales
+ *                   are always round-to-nearest-even).  SR draws 8 bits per
+ *                   element from Philox4x32-10 keyed by `seed`, counter
+ *                   ((t*H + h)/16, 0, stream 0, 0).
+ * Numerics: A_t = max|x|; k = smallest integer >= -126 with A_t <= 2688*2^k;
+ * s_b = E4M3_RNE(max|x_block| / (6*S_t)); code = E2M1(x / (s_b*S_t)), nearest
+ * with ties to even, saturating at 6, sign kept (also for zero).
+ */
+ep_status ep_nvfp4_pack(const void *tokens_bf16, int64_t T, int64_t H,
+                        const int32_t *dest, int k,
+                        const int32_t *expert_offsets,
+                        const int32_t *expert_counts, int E, uint8_t *rows,
+                        int64_t R_cap, int rounding, uint64_t seed,
+                        uint32_t *dev_status, void *stream);
+
+/*
+ * ep_nvfp4_unpack -- decode packed rows to BF16 (the path used when direct
+ * receive is off).  TE PR #3753, PR description: "Otherwise the rows are
+ * decoded to BF16"; commit "grad direct-receive opt-out": the opt-out returns
+ * the BF16 decode of the received rows.
+ *   rows            device u8 [R_cap, S] (ep_nvfp4_pack layout).
+ *   out_bf16        device bf16 [R_cap, H]; rows [0, R) written with
+ *                   BF16(sign * E2M1 value * s_b * S_t) (exact in BF16 except
+ *                   below its normal range, where it is rounded to nearest).
+ */
+ep_status ep_nvfp4_unpack(const uint8_t *rows, int64_t R_cap, int64_t H,
+                          const int32_t *expert_offsets, int E, void *out_bf16,
+                          uint32_t *dev_status, void *stream);
+
+/* Outputs of ep_nvfp4_direct_receive (all device memory). */
+typedef struct {
+    uint8_t *rw_codes;      /* u8 [R_cap, H/2]  rowwise codes (sender's)      */
+    uint8_t *rw_scales;     /* u8 [R_cap, H/16] rowwise E4M3 block scales     */
+    float *rw_row_scale;    /* f32 [R_cap]      per-row FP32 scale S_t        */
+    uint8_t *cw_codes;      /* u8 [R_cap*H/2]  columnwise RHT codes; expert e:
+                               [H][n_e/2] bytes at byte offsets[e]*H/2, the
+                               rows (tokens) of column h along the bytes     */
+    uint8_t *cw_scales;     /* u8 [R_cap*H/16] columnwise E4M3 scales; expert
+                               e: [H][n_e/16] at byte offsets[e]*H/16        */
+    float *amax_row;        /* f32 [E] rowwise amax of each expert            */
+    float *amax_col;        /* f32 [E] columnwise amax bound = 4 * amax_row   */
+    float *cw_scale_enc;    /* f32 [E] columnwise encode scale S_enc          */
+} ep_nvfp4_grouped;
+
+/*
+ * ep_nvfp4_direct_receive -- build the expert GEMM's grouped NVFP4 operands
+ * straight from the packed rows, in one pass over them.
+ * TE PR #3753, PR description: "the rowwise operand reuses the sender's codes
+ * and the columnwise RHT operand is quantized with a bound-derived per-expert
+ * scale, so no BF16 round trip or amax pass is needed"; TE PR #3755, PR
+ * description: "the post-RHT columnwise amax is bounded by 4x the rowwise
+ * amax"; TE PR #3324, description: row-scaled (per-token) NVFP4 operands.
+ *   rows            device u8 [R_cap, S].
+ *   out             host pointer to the output descriptor.  The rowwise group
+ *                   (rw_codes, rw_scales, rw_row_scale) may be all NULL to skip
+ *                   it; everything else is required.
+ *   rounding, seed  columnwise element rounding; SR counter = (p/16, 0,
+ *                   stream 1, 0) with p = offsets[e]*H + h*n_e + row-in-expert.
+ *   rht_sign_mask   bit i set = sign -1 on the i-th row of every 16-row block.
+ * Per expert: amax_row = max of the rows' token amaxes; amax_col = 4*amax_row;
+ * S_enc = min(2688/amax_col, FLT_MAX) (1 if amax_col = 0).  Per hidden column
+ * and 16-row block: y = (1/4) H16 diag(sigma) d over the decoded values d;
+ * s = E4M3_RNE_sat(max|y| * (S_enc/6)); code = E2M1(|y| * (S_enc/s)) with the
+ * sign of y (FP32, single-rounded operations, in this order).
+ * Two kernels (per-expert amax, then the tiled transform).
+ */
+ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
+                                  int64_t H, const int32_t *expert_offsets,
+                                  int E, const ep_nvfp4_grouped *out,
+                                  int rounding, uint64_t seed,
+                                  uint16_t rht_sign_mask, uint32_t *dev_status,
+                                  void *stream);
+
+/*
+ * ep_mxfp8_pack -- MXFP8 variant of the pack with the same routing gather.
+ * TE PR #3270, description: bfloat16 tokens are quantised to MXFP8 and
+ * dispatched; sequence diagram: "Quantize to E4M3 + E8M0 scales"; Changes:
+ * "recv data and block scales share a single caller-supplied buffer, sliced
+ * into data-then-scale regions".
+ *   buf             device u8: data [R_cap, H] then scales [R_cap, H/32].
+ * Per 32-element block: e = smallest integer in [-127, 127] with
+ * max|x| <= 448*2^e, scale byte e + 127, element E4M3_RNE(x / 2^e).
+ * Padding rows are all zero (data and scale bytes).
+ */
+ep_status ep_mxfp8_pack(const void *tokens_bf16, int64_t T, int64_t H,
+                        const int32_t *dest, int k,
+                        const int32_t *expert_offsets,
+                        const int32_t *expert_counts, int E, uint8_t *buf,
+                        int64_t R_cap, uint32_t *dev_status, void *stream);
+
+/* Human-readable name of a status code. */
+const char *ep_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EPQ_H */

@@ -1,0 +1,173 @@
+"""Python binding of libepq.so: argument marshalling only.
+
+Each function takes torch CUDA tensors, allocates outputs the caller did not
+pass (torch is the allocator; the library never allocates), and calls the C
+entry point of the same name on the current torch stream.  Every step of the
+path runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import EP_ROUND_RNE, EP_ROUND_SR, EpGrouped, check
+
+DEFAULT_ALIGNMENT = 128
+DEFAULT_SIGN_MASK = 0xA53C
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def row_bytes(H: int) -> int:
+    return int(_lib.lib().ep_nvfp4_row_bytes(int(H)))
+
+
+def rows_capacity(T: int, k: int, E: int, A: int = DEFAULT_ALIGNMENT) -> int:
+    return int(_lib.lib().ep_rows_capacity(int(T), int(k), int(E), int(A)))
+
+
+@dataclass
+class RoutePlan:
+    """Device-resident routing plan (all int32 CUDA tensors)."""
+    offsets: torch.Tensor     # [E+1]
+    counts: torch.Tensor      # [E]
+    dest: torch.Tensor        # [T*k]
+    T: int
+    k: int
+    E: int
+    A: int
+    R_cap: int
+    status: torch.Tensor      # uint32-valued int32 [1], EP_DEV_ERR_* bits
+
+
+def new_status(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def ep_route_plan(topk_idx: torch.Tensor, E: int, A: int = DEFAULT_ALIGNMENT, R_cap: int | None = None,
+                  plan: RoutePlan | None = None, workspace: torch.Tensor | None = None,
+                  status: torch.Tensor | None = None, stream=None) -> RoutePlan:
+    """Place every (token, slot) of ``topk_idx`` [T, k] (int32, -1 = dropped)
+    in expert-contiguous, A-aligned row order."""
+    _need_cuda(topk_idx, "topk_idx", torch.int32)
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    if R_cap is None:
+        R_cap = rows_capacity(T, k, E, A)
+    if plan is None:
+        plan = RoutePlan(torch.empty(E + 1, dtype=torch.int32, device=dev),
+                         torch.empty(E, dtype=torch.int32, device=dev),
+                         torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+                         T, k, E, A, R_cap, status if status is not None else new_status(dev))
+    ws_bytes = int(_lib.lib().ep_route_workspace_bytes(T, k, E))
+    if workspace is None:
+        workspace = torch.empty((ws_bytes + 3) // 4, dtype=torch.int32, device=dev)
+    st = _lib.lib().ep_route_plan(_ptr(topk_idx), T, k, E, A, R_cap, _ptr(plan.offsets), _ptr(plan.counts),
+                                  _ptr(plan.dest), _ptr(workspace), workspace.numel() * 4, _ptr(plan.status),
+                                  _stream(stream))
+    check("ep_route_plan", st)
+    return plan
+
+
+def ep_nvfp4_pack(tokens: torch.Tensor, plan: RoutePlan, rows: torch.Tensor | None = None,
+                  rounding: int = EP_ROUND_RNE, seed: int = 0, stream=None) -> torch.Tensor:
+    """BF16 tokens [T, H] -> packed NVFP4 rows [R_cap, row_bytes(H)] (uint8)."""
+    _need_cuda(tokens, "tokens", torch.bfloat16)
+    T, H = tokens.shape
+    S = row_bytes(H)
+    if rows is None:
+        rows = torch.empty((plan.R_cap, S), dtype=torch.uint8, device=tokens.device)
+    _need_cuda(rows, "rows", torch.uint8)
+    st = _lib.lib().ep_nvfp4_pack(_ptr(tokens), T, H, _ptr(plan.dest), plan.k, _ptr(plan.offsets),
+                                  _ptr(plan.counts), plan.E, _ptr(rows), rows.shape[0], int(rounding),
+                                  int(seed) & ((1 << 64) - 1), _ptr(plan.status), _stream(stream))
+    check("ep_nvfp4_pack", st)
+    return rows
+
+
+def ep_nvfp4_unpack(rows: torch.Tensor, H: int, offsets: torch.Tensor, E: int,
+                    out: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Packed rows -> BF16 [R_cap, H]; rows [0, offsets[E]) are written."""
+    _need_cuda(rows, "rows", torch.uint8)
+    R_cap = rows.shape[0]
+    if out is None:
+        out = torch.empty((R_cap, H), dtype=torch.bfloat16, device=rows.device)
+    if status is None:
+        status = new_status(rows.device)
+    st = _lib.lib().ep_nvfp4_unpack(_ptr(rows), R_cap, H, _ptr(offsets), E, _ptr(out), _ptr(status),
+                                    _stream(stream))
+    check("ep_nvfp4_unpack", st)
+    return out
+
+
+def alloc_grouped(R_cap: int, H: int, E: int, device, rowwise: bool = True) -> dict:
+    u8, f32 = torch.uint8, torch.float32
+    g = dict(cw_codes=torch.empty(R_cap * H // 2, dtype=u8, device=device),
+             cw_scales=torch.empty(R_cap * H // 16, dtype=u8, device=device),
+             amax_row=torch.empty(E, dtype=f32, device=device),
+             amax_col=torch.empty(E, dtype=f32, device=device),
+             cw_scale_enc=torch.empty(E, dtype=f32, device=device))
+    if rowwise:
+        g.update(rw_codes=torch.empty((R_cap, H // 2), dtype=u8, device=device),
+                 rw_scales=torch.empty((R_cap, H // 16), dtype=u8, device=device),
+                 rw_row_scale=torch.empty(R_cap, dtype=f32, device=device))
+    return g
+
+
+def grouped_struct(g: dict) -> EpGrouped:
+    return EpGrouped(*[ctypes.c_void_p(g[n].data_ptr()) if g.get(n) is not None else None
+                       for n, _ in EpGrouped._fields_])
+
+
+def ep_nvfp4_direct_receive(rows: torch.Tensor, H: int, offsets: torch.Tensor, E: int,
+                            out: dict | None = None, rounding: int = EP_ROUND_RNE, seed: int = 0,
+                            sign_mask: int = DEFAULT_SIGN_MASK, status: torch.Tensor | None = None,
+                            rowwise: bool = True, stream=None) -> dict:
+    """Packed rows -> grouped rowwise + columnwise-RHT NVFP4 operands (dict of
+    tensors, see ep_nvfp4_grouped in include/epq.h)."""
+    _need_cuda(rows, "rows", torch.uint8)
+    R_cap = rows.shape[0]
+    if out is None:
+        out = alloc_grouped(R_cap, H, E, rows.device, rowwise)
+    if status is None:
+        status = new_status(rows.device)
+    desc = grouped_struct(out)
+    st = _lib.lib().ep_nvfp4_direct_receive(_ptr(rows), R_cap, H, _ptr(offsets), E, ctypes.byref(desc),
+                                            int(rounding), int(seed) & ((1 << 64) - 1), int(sign_mask) & 0xFFFF,
+                                            _ptr(status), _stream(stream))
+    check("ep_nvfp4_direct_receive", st)
+    return out
+
+
+def ep_mxfp8_pack(tokens: torch.Tensor, plan: RoutePlan, buf: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """BF16 tokens -> one uint8 buffer: data [R_cap, H] then scales [R_cap, H/32]."""
+    _need_cuda(tokens, "tokens", torch.bfloat16)
+    T, H = tokens.shape
+    if buf is None:
+        buf = torch.empty(plan.R_cap * H + plan.R_cap * (H // 32), dtype=torch.uint8, device=tokens.device)
+    st = _lib.lib().ep_mxfp8_pack(_ptr(tokens), T, H, _ptr(plan.dest), plan.k, _ptr(plan.offsets),
+                                  _ptr(plan.counts), plan.E, _ptr(buf), plan.R_cap, _ptr(plan.status),
+                                  _stream(stream))
+    check("ep_mxfp8_pack", st)
+    return buf

@@ -1,0 +1,289 @@
+// Device-side building blocks shared by the epq kernels: format conversions
+// (inline PTX cvt forms of sm_100-family GPUs), packed FP32 pair arithmetic,
+// mbarrier / TMA / programmatic-dependent-launch wrappers, and the
+// Philox4x32-10 generator used for stochastic rounding.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace epq {
+
+constexpr uint32_t kDevErrBadExpert = 1u;
+constexpr uint32_t kDevErrDupExpert = 2u;
+constexpr uint32_t kDevErrTimeout = 4u;
+constexpr uint32_t kDevErrCapacity = 8u;
+
+// ---------------------------------------------------------------- bit casts
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+// 2^k as FP32 for k in [-126, 127].
+__device__ __forceinline__ float exp2i(int k) { return u2f((uint32_t)(k + 127) << 23); }
+
+// ---------------------------------------------------------------- E2M1 / E4M3
+// Two FP32 values -> one byte holding two E2M1 codes, round to nearest even,
+// saturating at +-6.  `lo` lands in the low nibble (the even element).
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u16.u8 %0, t;\n\t}"
+        : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One byte of two E2M1 codes -> f16x2 (exact); the low nibble goes to the low
+// half.
+__device__ __forceinline__ uint32_t cvt_f16x2_from_e2m1x2(uint32_t byte)
+{
+    uint32_t r;
+    uint16_t b = (uint16_t)byte;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "mov.b16 {t, _}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(r) : "h"(b));
+    return r;
+}
+
+// Two FP32 values -> two E4M3 codes (round to nearest even, saturating at
+// +-448); `lo` in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two E4M3 codes (low byte first) -> f16x2, exact.
+__device__ __forceinline__ uint32_t cvt_f16x2_from_e4m3x2(uint32_t two)
+{
+    uint32_t r;
+    uint16_t b = (uint16_t)two;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(b));
+    return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h)
+{
+    __half2 v = *reinterpret_cast<__half2 *>(&h);
+    return __half22float2(v);
+}
+
+// E4M3 code -> FP32 (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code)
+{
+    return f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(code & 0xffu)).x;
+}
+
+// Two FP32 -> packed bf16x2, round to nearest even; `lo` in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ---------------------------------------------------------------- FP32 pairs
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+// a - b, one rounding: fma(b, -1, a).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible; allow the next kernel to be
+// scheduled.  Both are no-ops when the launch carries no programmatic edge.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- status
+__device__ __forceinline__ void raise_status(uint32_t *st, uint32_t bits)
+{
+    if (st)
+        atomicOr(st, bits);
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase of an mbarrier.  Gives up after roughly a second
+// (the try_wait instruction itself suspends for a while on each attempt) and
+// returns false; the caller records EP_DEV_ERR_TIMEOUT and unwinds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (i > 64)
+            __nanosleep(256);
+    }
+    return false;
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)m) : "memory");
+}
+
+// 2-D tiled load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m, int x, int y,
+                                            uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(smem_u32(smem_dst)), "l"((uint64_t)m), "r"(x), "r"(y), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 2-D tiled store shared -> global (elements outside the tensor are skipped).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, int x, int y, const void *smem_src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"((uint64_t)m), "r"(x), "r"(y), "r"(smem_u32(smem_src)) : "memory");
+}
+
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void tma_store_wait_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk store has completed.
+__device__ __forceinline__ void tma_store_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Named barrier over a subset of the CTA's warps.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads;
+// every participant gets the same result.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred)
+{
+    uint32_t out;
+    asm volatile("{\n\t.reg .pred pi, po;\n\t"
+                 "setp.ne.u32 pi, %1, 0;\n\t"
+                 "bar.red.or.pred po, %2, %3, pi;\n\t"
+                 "selp.u32 %0, 1, 0, po;\n\t}"
+                 : "=r"(out) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
+    return out != 0;
+}
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC'11): ten rounds, each two 32x32->64-bit products of words 0
+// and 2 with the round multipliers, the high halves XORed with the other two
+// words and the round key; the key is advanced by the Weyl constants between
+// rounds.
+struct Philox4 {
+    uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        c1 = (uint32_t)p1;
+        c3 = (uint32_t)p0;
+        c0 = n0;
+        c2 = n2;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return Philox4{c0, c1, c2, c3};
+}
+
+// The 16 random bytes of the aligned group of 16 elements starting at element
+// index idx0 (idx0 % 16 == 0) of stream `stream`: byte i of the result (word
+// i/4, byte i%4, little-endian) belongs to element idx0 + i.
+__device__ __forceinline__ Philox4 sr_bytes16(uint64_t seed, uint32_t stream, uint64_t idx0)
+{
+    uint64_t n = idx0 >> 4;
+    return philox4x32_10((uint32_t)n, (uint32_t)(n >> 32), stream, 0u, (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
+}
+
+// Stochastic rounding of an FP32 value onto the E2M1 grid with an 8-bit random
+// number r (0..255): with lo <= |v| < hi the neighbouring grid values, the
+// result is hi iff r + floor(256 (|v| - lo) / (hi - lo)) >= 256.  Returns the
+// grid value (exactly representable) with the sign of v; values >= 6 in
+// magnitude are returned as is (the saturating E2M1 conversion maps them to
+// +-6).  On [1, 6) the grid keeps one mantissa bit, so adding r below that bit
+// and truncating carries with exactly that probability; on [0, 1) the same is
+// done on 1 + |v| (added toward zero, so the fraction bits are the floor of
+// |v| * 2^23) where the grid step is 0.5 = one mantissa bit of [1, 2).
+__device__ __forceinline__ float sr_e2m1_value(float v, uint32_t r)
+{
+    uint32_t bits = f2u(v);
+    uint32_t sign = bits & 0x80000000u;
+    float a = u2f(bits & 0x7fffffffu);
+    uint32_t radd = r << 14;
+    float out;
+    if (a >= 6.0f) {
+        out = a;
+    } else if (a >= 1.0f) {
+        out = u2f((f2u(a) + radd) & 0xffc00000u);
+    } else {
+        uint32_t z = f2u(__fadd_rz(a, 1.0f));
+        uint32_t idx = ((z + radd) >> 22) - 254u; // 0, 1 or 2
+        out = (float)idx * 0.5f;
+    }
+    return u2f(f2u(out) | sign);
+}
+
+} // namespace epq

@@ -1,0 +1,91 @@
+// Host-side declarations shared by the epq translation units: kernel
+// launchers (one per kernel family) and launch helpers.  The extern "C"
+// boundary that validates arguments lives in api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace epq {
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    int device;
+    int num_sms;
+};
+
+// Launch `kernel` with programmatic stream serialization (PDL) so that its
+// launch latency overlaps the tail of the preceding kernel; every epq kernel
+// calls griddepcontrol.wait before it reads memory another kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Sets the dynamic shared-memory limit of `kernel` once per device (it is a
+// per-function attribute; setting it again inside a stream capture is avoided).
+template <typename K>
+cudaError_t ensure_smem_limit(K kernel, int device, int bytes, int *done_mask_words /*[2]*/)
+{
+    const int w = device >> 5, b = device & 31;
+    if (device >= 0 && device < 64 && (done_mask_words[w] >> b) & 1)
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && device >= 0 && device < 64)
+        done_mask_words[w] |= (1 << b);
+    return e;
+}
+
+size_t route_workspace_bytes(int64_t T, int E);
+cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, int k, int E, int A,
+                              int32_t *offsets, int32_t *counts, int32_t *dest, int32_t *hist,
+                              uint32_t *status);
+
+cudaError_t launch_nvfp4_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
+                              const int32_t *dest, int k, const int32_t *offsets,
+                              const int32_t *counts, int E, uint8_t *rows, int R_cap,
+                              int rounding, uint64_t seed, uint32_t *status);
+
+cudaError_t launch_mxfp8_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
+                              const int32_t *dest, int k, const int32_t *offsets,
+                              const int32_t *counts, int E, uint8_t *buf, int R_cap,
+                              uint32_t *status);
+
+cudaError_t launch_nvfp4_unpack(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
+                                const int32_t *offsets, int E, uint16_t *out, uint32_t *status);
+
+struct GroupedOut {
+    uint8_t *rw_codes;
+    uint8_t *rw_scales;
+    float *rw_row_scale;
+    uint8_t *cw_codes;
+    uint8_t *cw_scales;
+    float *amax_row;
+    float *amax_col;
+    float *scale_enc;
+};
+
+cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
+                                  const int32_t *offsets, int E, const GroupedOut &out,
+                                  int rounding, uint64_t seed, uint32_t sign_mask,
+                                  uint32_t *status);
+
+// Bytes of a packed NVFP4 row: roundup16(9H/16 + 16).
+inline int64_t row_bytes(int64_t H) { return (9 * H / 16 + 16 + 15) / 16 * 16; }
+
+} // namespace epq

@@ -1,0 +1,100 @@
+"""The C-ABI library loads and exports every symbol include/epq.h declares;
+host-side validation rejects bad arguments before anything is enqueued (no
+GPU is needed for these: every call here fails its checks before touching
+CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_quantization_gb300 as nq
+from nvfp4_quantization_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "epq.h")
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails a host check first
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_exported_symbols():
+    assert declared_functions() == sorted(_lib.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    L = nq.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_size_helpers():
+    L = nq.lib()
+    for H in (32, 1024, 1056, 4096, 7168):
+        assert L.ep_nvfp4_row_bytes(H) == ((9 * H // 16 + 16 + 15) // 16) * 16
+        assert L.ep_nvfp4_row_bytes(H) % 16 == 0
+    assert L.ep_rows_capacity(4096, 2, 16, 128) == 4096 * 2 + 16 * 127
+    assert L.ep_route_workspace_bytes(0, 2, 16) >= 16
+    assert L.ep_route_workspace_bytes(16384, 8, 256) == 32 * 256 * 4
+
+
+def test_status_strings():
+    for s in range(0, -8, -1):
+        assert _lib.status_string(s).startswith("EP_")
+
+
+def test_route_plan_validation():
+    L = nq.lib()
+    f = L.ep_route_plan
+    ok = dict(topk=FAKE, T=10, k=2, E=4, A=128, R_cap=10 * 2 + 4 * 127, off=FAKE, cnt=FAKE, dest=FAKE,
+              ws=FAKE, ws_bytes=1 << 20, st=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["topk"], a["T"], a["k"], a["E"], a["A"], a["R_cap"], a["off"], a["cnt"], a["dest"], a["ws"],
+                 a["ws_bytes"], a["st"], None)
+    assert call(off=None) == -1
+    assert call(st=None) == -1
+    assert call(k=0) == -2 and call(k=33) == -2 and call(E=0) == -2 and call(E=1025) == -2
+    assert call(T=-1) == -2
+    assert call(A=64) == -3 and call(A=0) == -3 and call(A=200) == -3
+    assert call(R_cap=10 * 2 + 4 * 127 - 1) == -4
+    assert call(ws_bytes=0) == -4
+
+
+def test_pack_validation():
+    L = nq.lib()
+
+    def call(**kw):
+        a = dict(tok=FAKE, T=4, H=1024, dest=FAKE, k=2, off=FAKE, cnt=FAKE, E=4, rows=FAKE, R_cap=600,
+                 rnd=0, seed=0, st=FAKE)
+        a.update(kw)
+        return L.ep_nvfp4_pack(a["tok"], a["T"], a["H"], a["dest"], a["k"], a["off"], a["cnt"], a["E"], a["rows"],
+                               a["R_cap"], a["rnd"], a["seed"], a["st"], None)
+    assert call(rows=None) == -1
+    assert call(H=1000) == -2 and call(H=0) == -2 and call(k=40) == -2
+    assert call(R_cap=-1) == -4
+    assert call(tok=ctypes.c_void_p(0x10008)) == -3
+    # MXFP8 shares the checks
+    assert L.ep_mxfp8_pack(FAKE, 4, 48, FAKE, 2, FAKE, FAKE, 4, FAKE, 600, FAKE, None) == -2
+
+
+def test_receive_and_unpack_validation():
+    L = nq.lib()
+    g = _lib.EpGrouped()
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, ctypes.byref(g), 0, 0, 0, FAKE, None) == -1
+    g = _lib.EpGrouped(rw_codes=FAKE.value, cw_codes=FAKE.value, cw_scales=FAKE.value, amax_row=FAKE.value,
+                       amax_col=FAKE.value, cw_scale_enc=FAKE.value)
+    # a partial rowwise group is rejected
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, ctypes.byref(g), 0, 0, 0, FAKE, None) == -1
+    g.rw_codes = None
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1000, FAKE, 4, ctypes.byref(g), 0, 0, 0, FAKE, None) == -2
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, ctypes.byref(g), 7, 0, 0, FAKE, None) == -5
+    assert L.ep_nvfp4_unpack(FAKE, 128, 1000, FAKE, 4, FAKE, FAKE, None) == -2
+    assert L.ep_nvfp4_unpack(None, 128, 1024, FAKE, 4, FAKE, FAKE, None) == -1

@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, bit for bit (codes, scales, metadata, decoded BF16,
+MXFP8 bytes, routing).  Sizes here are ones the oracle finishes in seconds
+while still spanning several tiles and a ragged tail; the full-size configs
+are in test_gpu_fullsize.py."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_quantization_gb300 as nq
+import oracle
+import workloads
+from paths import CANARY, GpuRun, OracleRun, assert_bytes_equal, compare_runs, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+CASES = {
+    "cfg1": dict(cfg=1, kw={}, unpack=True),
+    "cfg2": dict(cfg=2, kw=dict(T=600, H=1024), unpack=False),
+    "cfg3": dict(cfg=3, kw=dict(T=700, H=2048), unpack=True),
+    "cfg4": dict(cfg=4, kw=dict(T=300, H=1024, E=64, k=8), unpack=False),
+    "cfg5": dict(cfg=5, kw=dict(T=400, H=1024), unpack=False, mxfp8=True),
+    "cfg1_ragged_H": dict(cfg=1, kw=dict(T=130, H=1056), unpack=True, mxfp8=True),
+    "cfg4_ragged_H": dict(cfg=4, kw=dict(T=90, H=288, E=16, k=4), unpack=True, mxfp8=True),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_parity_config(name):
+    c = CASES[name]
+    w = workloads.make(c["cfg"], **c["kw"])
+    g = GpuRun(w, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False))
+    o = OracleRun(w, g.R_cap, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False))
+    compare_runs(g, o)
+
+
+def test_parity_rne_and_sr_on_same_tokens():
+    base = workloads.make(4, T=200, H=512, E=16, k=4)
+    for rounding, seed in ((0, 0), (1, 1), (1, 0xFFFFFFFFFFFF1234)):
+        base.rounding, base.seed = rounding, seed
+        g = GpuRun(base)
+        o = OracleRun(base, g.R_cap)
+        compare_runs(g, o)
+
+
+def test_parity_without_rowwise_outputs():
+    w = workloads.make(2, T=300, H=512)
+    g = GpuRun(w, rowwise=False)
+    o = OracleRun(w, g.R_cap)
+    compare_runs(g, o, check_rowwise=False)
+
+
+def special_tokens(H=512):
+    """Tokens that reach every branch of the encoder: the fast and the slow
+    division paths (tiny and huge token scales, the -126 floor), zero tokens,
+    negative zeros, exact ties, saturation."""
+    rng = np.random.default_rng(9)
+    rows = []
+    for scale in (1.0, 1e-30, 1e30, 3e-37, 1e-38, 2.0 ** -110, 2.0 ** 105, 3.0e37):
+        x = rng.standard_normal(H).astype(np.float32) * np.float32(scale)
+        rows.append(x)
+    rows.append(np.zeros(H, np.float32))
+    z = np.zeros(H, np.float32)
+    z[::3] = -0.0
+    rows.append(z)
+    ties = np.tile(np.array([6, 1, 0.5, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -5, -0.25, 4.5, 0, -0.0, 3],
+                            np.float32), H // 16)
+    rows.append(ties)
+    rows.append(ties * np.float32(2.0 ** -100))
+    one = np.zeros(H, np.float32)
+    one[7] = -3.0
+    rows.append(one)
+    return workloads.to_bf16_bits(np.stack(rows))
+
+
+def test_parity_special_tokens_and_routing_edges():
+    tokens = special_tokens()
+    T = tokens.shape[0]
+    topk = np.array([[i % 5, (i + 2) % 5] for i in range(T)], np.int32)
+    topk[1, 1] = -1           # dropped slot
+    topk[2, 1] = 9            # id out of range -> status bit, dropped
+    topk[3, 1] = topk[3, 0]   # repeated id -> status bit, later slot dropped
+    w = workloads.Workload("special", "special", tokens, topk, E=5)
+    g = GpuRun(w, unpack=True, mxfp8=True)
+    o = OracleRun(w, g.R_cap, unpack=True, mxfp8=True)
+    assert o.status == 3
+    compare_runs(g, o)
+
+
+def test_parity_empty_and_single_token():
+    for T, E in ((0, 4), (1, 1), (1, 8)):
+        rng = np.random.default_rng(T + E)
+        tokens = workloads.to_bf16_bits(rng.standard_normal((T, 256)).astype(np.float32))
+        k = min(2, E)
+        topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else \
+            np.zeros((0, k), np.int32)
+        w = workloads.Workload("edge", "edge", tokens, topk, E=E)
+        g = GpuRun(w, unpack=True, mxfp8=True)
+        o = OracleRun(w, g.R_cap, unpack=True, mxfp8=True)
+        compare_runs(g, o)
+
+
+def test_parity_all_slots_dropped_and_one_hot_expert():
+    rng = np.random.default_rng(3)
+    tokens = workloads.to_bf16_bits(rng.standard_normal((700, 256)).astype(np.float32))
+    topk = np.full((700, 2), -1, np.int32)
+    w = workloads.Workload("dropped", "dropped", tokens, topk, E=3)
+    g = GpuRun(w)
+    o = OracleRun(w, g.R_cap)
+    compare_runs(g, o)
+    topk = np.zeros((700, 1), np.int32) + 2   # every token to expert 2, 700 rows -> ragged 768
+    w = workloads.Workload("hot", "hot", tokens, topk, E=3, A=256)
+    g = GpuRun(w, unpack=True)
+    o = OracleRun(w, g.R_cap, unpack=True)
+    compare_runs(g, o)
+
+
+def exhaustive_encode_tokens(token_scale_exp: int, H=2048):
+    """Blocks whose max fixes every positive E4M3 block scale s_b (B = 6 s_b S_t)
+    filled with every BF16 magnitude in [2^-10 s, 6 s] (both signs): every
+    (value, block scale) pair of the encoder's decision range appears."""
+    St = 2.0 ** token_scale_exp
+    e4 = torch.arange(127, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    allbf = (np.arange(1 << 15, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    allbf = allbf[np.isfinite(allbf)]
+    blocks = []
+    for code in range(1, 127):
+        s = e4[code] * St
+        B = 6.0 * s
+        vals = allbf[(allbf >= s * 2.0 ** -10) & (allbf <= B)]
+        vals = np.concatenate([vals, -vals])
+        n = len(vals)
+        nb = -(-n // 15)
+        pad = np.resize(vals, nb * 15).reshape(nb, 15)
+        blk = np.concatenate([np.full((nb, 1), B), pad], axis=1)
+        blocks.append(blk)
+    blocks = np.concatenate(blocks)
+    per_tok = H // 16 - 1
+    ntok = -(-len(blocks) // per_tok)
+    blocks = np.resize(blocks, (ntok * per_tok, 16))
+    # first block of every token carries the token amax 2688 * S_t (S_t exact)
+    first = np.zeros((ntok, 16))
+    first[:, 0] = 2688.0 * St
+    tok = np.concatenate([first[:, None, :], blocks.reshape(ntok, per_tok, 16)], axis=1).reshape(ntok, H)
+    return workloads.to_bf16_bits(tok.astype(np.float32))
+
+
+@pytest.mark.parametrize("kexp", [0, -20, 12, -110, 105])
+def test_parity_exhaustive_encode(kexp):
+    tokens = exhaustive_encode_tokens(kexp)
+    T = tokens.shape[0]
+    topk = (np.arange(T, dtype=np.int32) % 4).reshape(T, 1)
+    for rounding in (0, 1):
+        w = workloads.Workload("exh", "exh", tokens, topk, E=4, rounding=rounding, seed=17)
+        g = GpuRun(w, unpack=True)
+        o = OracleRun(w, g.R_cap, unpack=True)
+        compare_runs(g, o)
+
+
+def test_deterministic_repeat():
+    w = workloads.make(4, T=200, H=512, E=16, k=4)
+    a = GpuRun(w, mxfp8=True, unpack=True)
+    b = GpuRun(w, mxfp8=True, unpack=True)
+    assert torch.equal(a.rows, b.rows)
+    for k in a.grouped:
+        assert torch.equal(a.grouped[k], b.grouped[k]), k
+    assert torch.equal(a.mx, b.mx) and torch.equal(a.unpacked.view(torch.int16), b.unpacked.view(torch.int16))
+
+
+def test_cuda_graph_capture_matches_eager():
+    """Route plan + pack + direct receive captured in one CUDA graph replay to
+    the same bytes as the eager calls (the library allocates nothing and never
+    synchronises, so every call is capturable)."""
+    w = workloads.make(2, T=500, H=1024)
+    eager = GpuRun(w)
+    tok = to_dev_bf16(w.tokens)
+    topk = torch.from_numpy(w.topk).cuda()
+    R_cap = eager.R_cap
+    plan = nq.ep_route_plan(topk, w.E, w.A, R_cap=R_cap)      # warm-up call, allocates outputs
+    ws = torch.empty(nq.lib().ep_route_workspace_bytes(w.T, w.k, w.E) // 4 + 1, dtype=torch.int32, device="cuda")
+    rows = torch.empty((R_cap, nq.row_bytes(w.H)), dtype=torch.uint8, device="cuda")
+    out = nq.alloc_grouped(R_cap, w.H, w.E, "cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            nq.ep_route_plan(topk, w.E, w.A, R_cap=R_cap, plan=plan, workspace=ws)
+            nq.ep_nvfp4_pack(tok, plan, rows=rows)
+            nq.ep_nvfp4_direct_receive(rows, w.H, plan.offsets, w.E, out=out, status=plan.status)
+    rows.fill_(CANARY)
+    for t in out.values():
+        t.view(torch.uint8).fill_(CANARY)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    R = int(plan.offsets[-1].item())
+    assert torch.equal(rows[:R], eager.rows[:R])
+    for k, v in out.items():
+        n = {"cw_codes": R * w.H // 2, "cw_scales": R * w.H // 16}.get(k)
+        ref = eager.grouped[k]
+        if k.startswith("rw"):
+            assert torch.equal(v[:R], ref[:R]), k
+        elif n is not None:
+            assert torch.equal(v[:n], ref[:n]), k
+        else:
+            assert torch.equal(v, ref), k
+
+
+def test_device_guard_follows_input_device():
+    """The call runs on the device of its input even when another device is
+    current (single-GPU machines: the current device is set to a different
+    value only if there is one)."""
+    w = workloads.make(1, T=64, H=256)
+    g = GpuRun(w)
+    assert g.status == 0
+    assert torch.cuda.current_device() == 0
