@@ -3,9 +3,9 @@
 Workload: 4096 tokens x 4096 hidden BF16 ~N(0,1) with 0.1% of entries x50;
 16 experts, softmax-of-Gaussian top-2 routing with 2 experts forced empty;
 alignment 128; round-to-nearest-even (the dispatch-forward configuration).
-A step is one pass of the whole path over one batch: route plan (2 kernels),
-NVFP4 pack with the routing gather (1 kernel), direct receive (per-expert
-amax + tiled rowwise / columnwise-RHT kernel).
+A step is one pass of the whole path over one batch: route plan (1 kernel),
+NVFP4 pack with the routing gather (1 kernel), direct receive (1 kernel:
+per-expert amax prologue + tiled rowwise / columnwise-RHT transform).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -49,6 +49,7 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--sets", type=int, default=N_SETS, help="rotating buffer sets (profiling uses 1)")
     return p.parse_args()
 
 
@@ -167,8 +168,7 @@ class BufferSet:
         self.tok = tok_host.cuda()
         self.topk = topk_host.cuda()
         self.plan = nq.ep_route_plan(self.topk, w.E, w.A)
-        ws_b = int(nq.lib().ep_route_workspace_bytes(w.T, w.k, w.E))
-        self.ws = torch.empty((ws_b + 3) // 4, dtype=torch.int32, device="cuda")
+        self.ws = nq.new_route_workspace(w.T, w.k, w.E, "cuda")
         self.rows = torch.empty((self.plan.R_cap, nq.row_bytes(w.H)), dtype=torch.uint8, device="cuda")
         self.out = nq.alloc_grouped(self.plan.R_cap, w.H, w.E, "cuda")
         self.w, self.nq = w, nq
@@ -188,14 +188,32 @@ class BufferSet:
     def capture(self, torch):
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
-        self.gA, self.gB = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        self.gA, self.gB, self.gS = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
             with torch.cuda.graph(self.gA, stream=s):
                 self.route_pack()
             with torch.cuda.graph(self.gB, stream=s):
                 self.receive()
+            with torch.cuda.graph(self.gS, stream=s):
+                self.route_pack()
+                self.receive()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
+
+
+def capture_rotation(torch, sets):
+    """One graph holding one step on every buffer set, in rotation order."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for b in sets:
+                b.route_pack()
+                b.receive()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
 
 
 def gpu_arm(args, rank, world, local):
@@ -218,7 +236,7 @@ def gpu_arm(args, rank, world, local):
     T, H, k, E = w.T, w.H, w.k, w.E
     tok_host = torch.from_numpy(w.tokens.view(np.int16)).view(torch.bfloat16)
     topk_host = torch.from_numpy(np.ascontiguousarray(w.topk))
-    sets = [BufferSet(torch, nq, w, tok_host, topk_host) for _ in range(N_SETS)]
+    sets = [BufferSet(torch, nq, w, tok_host, topk_host) for _ in range(args.sets)]
     torch.cuda.synchronize()
     st = int(sets[0].plan.status.item())
     if st != 0:
@@ -228,35 +246,42 @@ def gpu_arm(args, rank, world, local):
     for b in sets:
         b.capture(torch)
 
-    # ---- timed region: K steps, rotating buffer sets (cold L2 per step)
+    # ---- timed region: K steps, rotating buffer sets (cold L2 per step).
+    # Steps go in blocks of one step per set; one graph replay runs a whole
+    # block, so the host stays far ahead of the GPU.  Every SAMPLE_EVERY-th
+    # block is replayed kernel-group by kernel-group with CUDA events between
+    # them: those steps give the per-kernel durations of the roofline.
+    gR = capture_rotation(torch, sets)
     K, W = args.steps, args.warmup
-    every = max(1, K // 2000)
-    for i in range(W):
-        b = sets[i % N_SETS]
-        b.gA.replay()
-        b.gB.replay()
+    nset = len(sets)
+    SAMPLE_EVERY = 10
+    for i in range(max(1, W // nset)):
+        gR.replay()
     torch.cuda.synchronize()
     barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range((K + every - 1) // every)]
+    nblocks, rem = divmod(K, nset)
+    n_sampled = (nblocks + SAMPLE_EVERY - 1) // SAMPLE_EVERY
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(nset)] for _ in range(n_sampled)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     clocks.start()
     time.sleep(0.2)
     wall0 = time.perf_counter()
     t0.record()
-    for i in range(K):
-        b = sets[i % N_SETS]
-        if i % every == 0:
-            e = ev[i // every]
-            e[0].record()
-            b.gA.replay()
-            e[1].record()
-            b.gB.replay()
-            e[2].record()
+    for blk in range(nblocks):
+        if blk % SAMPLE_EVERY == 0:
+            for j, b in enumerate(sets):
+                e = ev[blk // SAMPLE_EVERY][j]
+                e[0].record()
+                b.gA.replay()
+                e[1].record()
+                b.gB.replay()
+                e[2].record()
         else:
-            b.gA.replay()
-            b.gB.replay()
+            gR.replay()
+    for j in range(rem):
+        sets[j].gS.replay()
     t1.record()
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
@@ -268,12 +293,14 @@ def gpu_arm(args, rank, world, local):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_total = float(tt.item())
     ms_step = ms_total / K
-    ms_a = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    ms_b = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    flat = [e for row in ev for e in row]
+    ms_a = float(np.mean([e[0].elapsed_time(e[1]) for e in flat]))
+    ms_b = float(np.mean([e[1].elapsed_time(e[2]) for e in flat]))
     st = int(sets[0].plan.status.item())
     route_b, pack_b, dr_b = algorithmic_bytes(T, H, k, E, R, S)
     res = dict(T=T, H=H, k=k, E=E, R=R, S=S, ms_step=ms_step, ms_a=ms_a, ms_b=ms_b, wall_s=wall1 - wall0,
-               clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), world=world, w=w)
+               clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), world=world, w=w,
+               n_sampled_steps=len(flat))
 
     # ---- end to end through the public API with host buffers
     res["e2e"] = e2e_measure(torch, nq, w, sets[0], tok_host, topk_host, R, args.e2e_steps)
@@ -395,19 +422,20 @@ def main():
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.description, "T": r["T"], "H": r["H"], "E": r["E"], "k": r["k"], "A": w.A,
-                   "R": r["R"], "rounding": "rne", "l2": f"{N_SETS} rotating buffer sets (inputs+outputs "
-                   f"> 4x L2), back-to-back CUDA-graph steps", "parallelism": f"replicas x{world}"},
+                   "R": r["R"], "rounding": "rne", "l2": f"{args.sets} rotating buffer sets (~94 MB each; "
+                   "a set is reused after the others pushed > 2x L2 through), back-to-back CUDA-graph steps", "parallelism": f"replicas x{world}"},
         "path": {"gbs": path_gbs, "frac_of_peak": path_gbs / peak, "bytes_per_step": route_b + pack_b + dr_b,
                  "route_pack_ms": r["ms_a"], "route_pack_gbs": pack_gbs, "direct_receive_ms": r["ms_b"],
                  "direct_receive_gbs": dr_gbs},
-        "roofline": {"kernel": "ep_nvfp4_direct_receive (expert amax + tiled transform)", "bound": "hbm",
+        "roofline": {"kernel": "direct_receive_kernel (ep_nvfp4_direct_receive)", "bound": "hbm",
                      "achieved": dr_gbs, "peak": peak, "unit": "GB/s", "frac": dr_gbs / peak,
                      "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": dr_b,
                      "traffic": profiled_traffic("direct_receive", DR_SOURCES)},
         "e2e": {"value": world * r["T"] / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"],
                 "api": "eager ep_route_plan / ep_nvfp4_pack / ep_nvfp4_direct_receive", "checked": e2e["ok"]},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 3 * args.steps,
+        "sampled_steps_for_kernel_times": r["n_sampled_steps"],
         "clocks": r["clocks"],
         "device_status": r["status"],
         "timed_wall_s": r["wall_s"],

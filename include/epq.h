@@ -77,8 +77,12 @@ size_t ep_nvfp4_row_bytes(int64_t H);
 /* Upper bound on R = sum_e ceil(c_e / A) * A over any routing: T*k + E*(A-1). */
 int64_t ep_rows_capacity(int64_t T, int k, int E, int A);
 
-/* Device workspace needed by ep_route_plan (ceil(T/1024) * E * 4 bytes, at
- * least 16). */
+/* Device workspace needed by ep_route_plan: 16 + ceil(T/512) * E * 4 bytes.
+ * Its first 16 bytes hold a grid-barrier count and generation: they must be
+ * zero before the workspace is first used, and every call that completes
+ * leaves them usable for the next call (a zero-filled buffer can be reused
+ * indefinitely by calls on one stream; calls that may overlap need separate
+ * workspaces). */
 size_t ep_route_workspace_bytes(int64_t T, int k, int E);
 
 /*
@@ -98,10 +102,13 @@ size_t ep_route_workspace_bytes(int64_t T, int k, int E);
  *                   n_e - c_e trailing rows of expert e are padding rows.
  *   dest            device int32 [T*k] out: row of (t, j), or -1 if dropped.
  *                   Within an expert, rows follow ascending token order.
- *   workspace       device, ws_bytes >= ep_route_workspace_bytes(T, k, E).
+ *   workspace       device, ws_bytes >= ep_route_workspace_bytes(T, k, E),
+ *                   zero-filled before its first use (see above).
  *   R_cap           capacity the rows buffers will have; must be at least
  *                   ep_rows_capacity(T, k, E, A) (EP_ERR_CAPACITY otherwise).
- * Two kernels; T = 0 is allowed (all offsets and counts 0).
+ * One cooperative launch (all CTAs resident, one grid barrier whose wait is
+ * bounded: EP_DEV_ERR_TIMEOUT if it gives up); T = 0 is allowed (all offsets
+ * and counts 0).
  */
 ep_status ep_route_plan(const int32_t *topk_idx, int64_t T, int k, int E, int A,
                         int64_t R_cap, int32_t *expert_offsets,
@@ -188,7 +195,9 @@ typedef struct {
  * and 16-row block: y = (1/4) H16 diag(sigma) d over the decoded values d;
  * s = E4M3_RNE_sat(max|y| * (S_enc/6)); code = E2M1(|y| * (S_enc/s)) with the
  * sign of y (FP32, single-rounded operations, in this order).
- * Two kernels (per-expert amax, then the tiled transform).
+ * One kernel: each CTA first reduces the row trailers of the experts its tiles
+ * belong to (4 bytes per row) while its first tile loads are in flight, then
+ * transforms its tiles.
  */
 ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
                                   int64_t H, const int32_t *expert_offsets,

@@ -63,6 +63,12 @@ def new_status(device) -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=device)
 
 
+def new_route_workspace(T: int, k: int, E: int, device) -> torch.Tensor:
+    """A zero-filled workspace for ep_route_plan (reusable across calls)."""
+    nbytes = int(_lib.lib().ep_route_workspace_bytes(int(T), int(k), int(E)))
+    return torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=device)
+
+
 def ep_route_plan(topk_idx: torch.Tensor, E: int, A: int = DEFAULT_ALIGNMENT, R_cap: int | None = None,
                   plan: RoutePlan | None = None, workspace: torch.Tensor | None = None,
                   status: torch.Tensor | None = None, stream=None) -> RoutePlan:
@@ -78,9 +84,8 @@ def ep_route_plan(topk_idx: torch.Tensor, E: int, A: int = DEFAULT_ALIGNMENT, R_
                          torch.empty(E, dtype=torch.int32, device=dev),
                          torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
                          T, k, E, A, R_cap, status if status is not None else new_status(dev))
-    ws_bytes = int(_lib.lib().ep_route_workspace_bytes(T, k, E))
     if workspace is None:
-        workspace = torch.empty((ws_bytes + 3) // 4, dtype=torch.int32, device=dev)
+        workspace = new_route_workspace(T, k, E, dev)
     st = _lib.lib().ep_route_plan(_ptr(topk_idx), T, k, E, A, R_cap, _ptr(plan.offsets), _ptr(plan.counts),
                                   _ptr(plan.dest), _ptr(workspace), workspace.numel() * 4, _ptr(plan.status),
                                   _stream(stream))

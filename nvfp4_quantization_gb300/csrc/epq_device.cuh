@@ -36,6 +36,23 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
     return r;
 }
 
+// Eight FP32 values -> one word of eight E2M1 codes (round to nearest even,
+// saturating); a[0] in the lowest nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float a0, float a1, float a2, float a3, float a4, float a5,
+                                               float a6, float a7)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+    return r;
+}
+
 // One byte of two E2M1 codes -> f16x2 (exact); the low nibble goes to the low
 // half.
 __device__ __forceinline__ uint32_t cvt_f16x2_from_e2m1x2(uint32_t byte)
@@ -87,6 +104,12 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi)
     return r;
 }
 
+// Four bytes (each in the low byte of its word) -> one word, b0 lowest.
+__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3)
+{
+    return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
 // ---------------------------------------------------------------- FP32 pairs
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 // a - b, one rounding: fma(b, -1, a).
@@ -104,6 +127,14 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- gpu-scope loads
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // ---------------------------------------------------------------- status
@@ -140,6 +171,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("{\n\t.reg .b64 st;\n\t"
                  "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Raise the transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
@@ -180,6 +218,29 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
                  " [%0], [%1, {%2, %3}], [%4];"
                  ::"r"(smem_u32(smem_dst)), "l"((uint64_t)m), "r"(x), "r"(y), "r"(smem_u32(bar))
                  : "memory");
+}
+
+// 1-D bulk copy global -> shared (src, dst 16-byte aligned, bytes % 16 == 0),
+// completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// Bring [gsrc, gsrc + bytes) into L2 (16-byte aligned, bytes % 16 == 0).  L2 is
+// the point of coherence, so a prefetch issued before the data's producer has
+// finished cannot return stale data to later loads.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 2-D tiled store shared -> global (elements outside the tensor are skipped).

@@ -1,5 +1,5 @@
 // Direct receive: packed NVFP4 rows -> the expert GEMM's grouped rowwise and
-// columnwise-RHT NVFP4 operands, in one pass over the rows.
+// columnwise-RHT NVFP4 operands, in one pass over the rows, in one kernel.
 //
 // TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR description:
 // the receiver builds the NVFP4 GroupedTensor straight from the rows in one
@@ -9,26 +9,29 @@
 // NVFP4 amaxes from the dGLU epilogue", PR description: the post-RHT
 // columnwise amax is bounded by 4x the rowwise amax.
 //
-// Kernel 1 (expert_amax): one CTA per expert reduces the 4-byte token amaxes
-// in the row trailers (the rows' data is not read) into amax_row, the 4x
-// bound amax_col and the encode scale S_enc.
+// Work unit: a tile of 128 rows x 256 hidden columns (a tile never straddles
+// two experts: expert slots are multiples of 128 rows).  Each persistent CTA
+// owns a contiguous range of tiles and walks it column-strip by column-strip
+// (consecutive tiles of a strip complete each other's columnwise output
+// sectors), so it meets only one or two experts.
 //
-// Kernel 2 (direct_receive): persistent CTAs walk tiles of 128 rows x 256
-// hidden columns (a tile never straddles two experts: expert slots are
-// multiples of 128 rows), row-tile-major so that concurrently running CTAs
-// share row trailers and complete each other's output sectors in L2.  One
-// producer thread streams tiles into a 4-stage shared-memory ring with 2-D
-// TMA loads (codes box 128 B x 128 rows, scales 16 B x 128, trailers
-// 16 B x 128).  The rowwise operand leaves straight from the ring with a TMA
-// store (codes) and 16-byte stores (scales, token scale).  Each of 128
-// consumer threads owns two adjacent hidden columns (one code byte per row):
-// it decodes 16 rows at a time exactly into FP32 pairs using a per-tile
-// table of (E4M3 block scale x token scale x sigma / 4), runs the 16-point
-// Walsh-Hadamard butterflies on packed FP32 pairs, derives the E4M3 block
-// scale from the expert's S_enc, re-encodes to E2M1 (RNE or Philox-driven
-// stochastic rounding) and keeps the 64 code bytes and 8 scale bytes of each
-// column in registers until the tile is done, then writes them as whole
-// 16-byte chunks of the [H][n_e] columnwise layout.
+// Producer warp: streams tiles into a 3-stage shared-memory ring with 2-D TMA
+// loads (codes 128 B x 128 rows, scales 16 B x 128, row trailers 16 B x 128).
+// While a tile's loads are in flight it finds the tile's expert and, the
+// first time the CTA meets that expert, reduces the expert's 4-byte token
+// amaxes from the row trailers (the rows' data is not read again) into the
+// encode scale S_enc; the tile's expert, offsets and S_enc go into the stage
+// before the stage's barrier is released.
+//
+// Consumer warps (8): the rowwise operand leaves straight from the ring (TMA
+// store of the codes; 16-byte stores of the scales and the token scale).  For
+// the columnwise operand each thread owns two adjacent hidden columns (one
+// code byte per row) and 64 of the 128 rows: it decodes 16 rows at a time
+// exactly into FP32 pairs with a per-tile table of (E4M3 block scale x token
+// scale x sigma / 4), runs the 16-point Walsh-Hadamard butterflies on packed
+// FP32 pairs, derives the E4M3 block scale from S_enc, re-encodes to E2M1
+// (RNE or Philox-driven stochastic rounding) and writes 16-byte chunks of the
+// [H][n_e] columnwise layout.
 #include <cudaTypedefs.h>
 #include <float.h>
 #include <string.h>
@@ -42,64 +45,43 @@ constexpr int kTileRows = 128;
 constexpr int kTileCols = 256;
 constexpr int kCodeBytes = kTileCols / 2;    // 128
 constexpr int kScaleBytes = kTileCols / 16;  // 16
-constexpr int kStages = 4;
-constexpr int kConsumers = 128;              // 4 warps, 2 columns per thread
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;    // + 1 producer warp
 constexpr uint32_t kStageTx = kTileRows * (kCodeBytes + kScaleBytes + 16);
-constexpr int kTabStride = kTileRows + 4;    // pad: 4 column blocks per warp hit distinct banks
+constexpr int kWarpRows = kTileRows / 2;     // rows of a tile one consumer warp handles
+constexpr int kWTabStride = kWarpRows + 2;   // float2 entries; pad: a warp's 4 column blocks hit distinct banks
+constexpr int kMaxExperts = 1024;
+constexpr int kSlots = 8;                    // experts per CTA with precomputed S_enc / s tables
+
+struct StageMeta {
+    int e, off, n, slot; // slot < 0: the expert's tables are computed per tile
+    float se, ce;        // S_enc and fl32(S_enc / 6)
+};
 
 struct __align__(128) DrSmem {
     uint8_t codes[kStages][kTileRows][kCodeBytes];
     uint8_t scales[kStages][kTileRows][kScaleBytes];
     uint32_t trailer[kStages][kTileRows][4];
-    float table[2][kScaleBytes][kTabStride];  // [buf][column block][row]
-    float rtab[2][128];                       // [buf][E4M3 code] -> S_enc / s
+    float2 wtab[kConsumerWarps][4][kWTabStride]; // per warp: [column block][row] decode scale, twice
+    float wrtab[kConsumerWarps][128];           // per warp: S_enc / s when the expert has no slot
+    float rtab[kSlots][128];                    // [slot][E4M3 code] -> fl32(S_enc / s)
+    StageMeta meta[kStages];
+    float se_cache[kMaxExperts];                // S_enc of the experts this CTA meets
+    int offs[kMaxExperts + 1];                  // expert_offsets, copied once
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int abort_flag;
     int consumed;
 };
 
-// --------------------------------------------------------------- kernel 1
-__global__ void __launch_bounds__(256)
-expert_amax_kernel(const uint8_t *__restrict__ rows, int R_cap, int64_t S,
-                   const int32_t *__restrict__ offsets, int E, float *__restrict__ amax_row,
-                   float *__restrict__ amax_col, float *__restrict__ scale_enc,
-                   uint32_t *__restrict__ status)
-{
-    __shared__ uint32_t wm[8];
-    pdl_launch_dependents();
-    pdl_wait();
-    const int e = blockIdx.x;
-    int lo = offsets[e], hi = offsets[e + 1];
-    if (hi > R_cap) {
-        if (threadIdx.x == 0)
-            raise_status(status, kDevErrCapacity);
-        hi = R_cap;
-    }
-    uint32_t m = 0; // token amaxes are non-negative: compare their bit patterns
-    for (int r = lo + threadIdx.x; r < hi; r += blockDim.x)
-        m = max(m, __ldg(reinterpret_cast<const uint32_t *>(rows + (int64_t)r * S + S - 12)));
-    m = __reduce_max_sync(0xffffffffu, m);
-    if ((threadIdx.x & 31) == 0)
-        wm[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int i = 1; i < 8; ++i)
-            m = max(m, wm[i]);
-        const float a = u2f(m);
-        const float ac = 4.0f * a;
-        float se = 1.0f;
-        if (ac > 0.0f)
-            se = fminf(__fdiv_rn(2688.0f, ac), FLT_MAX);
-        amax_row[e] = a;
-        amax_col[e] = ac;
-        scale_enc[e] = se;
-    }
-}
+// two CTAs per SM: each gets at most (228 KB - 2 x 1 KB reserved) / 2
+static_assert(sizeof(DrSmem) + 1024 <= 113 * 1024, "direct receive must fit two CTAs per SM");
 
-// --------------------------------------------------------------- kernel 2
 struct DrArgs {
+    const uint8_t *rows;
+    int64_t S;
     const int32_t *offsets;
     int E;
     int H;
@@ -109,24 +91,182 @@ struct DrArgs {
     float *rw_row_scale;
     uint8_t *cw_codes;
     uint8_t *cw_scales;
-    const float *scale_enc;
+    float *amax_row;
+    float *amax_col;
+    float *scale_enc;
     uint64_t seed;
     uint32_t sign_mask;
     uint32_t *status;
     int do_rowwise;
 };
 
-__device__ __forceinline__ int expert_of_row(const int32_t *offsets, int E, int row)
+// Tiles [lo, hi) of this CTA (a contiguous share of all tiles), visited
+// strip by strip: for each column strip, the CTA's row tiles in order.
+struct TileWalk {
+    int lo, hi, rt0, rt1, ns, st, rt;
+    __device__ __forceinline__ void init(int n_units, int n_strips)
+    {
+        const int64_t G = gridDim.x, b = blockIdx.x;
+        lo = (int)(b * n_units / G);
+        hi = (int)((b + 1) * n_units / G);
+        ns = n_strips;
+        rt0 = lo / ns;
+        rt1 = hi > lo ? (hi - 1) / ns : rt0 - 1;
+        st = 0;
+        rt = rt0 - 1;
+    }
+    // Advance to the next tile; false when the CTA's share is exhausted.
+    __device__ __forceinline__ bool next()
+    {
+        if (hi <= lo)
+            return false;
+        for (;;) {
+            if (++rt > rt1) {
+                rt = rt0;
+                if (++st >= ns)
+                    return false;
+            }
+            const int u = rt * ns + st;
+            if (u >= lo && u < hi)
+                return true;
+        }
+    }
+};
+
+// Last e with offs[e] <= row (offs in shared memory).
+__device__ __forceinline__ int expert_of_row(const int *offs, int E, int row)
 {
-    int lo = 0, hi = E - 1; // last e with offsets[e] <= row
+    int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(offsets + mid) <= row)
+        if (offs[mid] <= row)
             lo = mid;
         else
             hi = mid - 1;
     }
     return lo;
+}
+
+// Issue the TMA loads of the it-th tile into its stage (lane 0 only).
+__device__ __forceinline__ void issue_tile(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
+                                           const CUtensorMap *tmt, int s, int rt, int st)
+{
+    const int row0 = rt * kTileRows;
+    mbar_expect_tx(&sm.full[s], kStageTx);
+    tma_load_2d(&sm.codes[s][0][0], tmc, st * kCodeBytes, row0, &sm.full[s]);
+    tma_load_2d(&sm.scales[s][0][0], tms, st * kScaleBytes, row0, &sm.full[s]);
+    tma_load_2d(&sm.trailer[s][0][0], tmt, 0, row0, &sm.full[s]);
+}
+
+// First min(kStages, tiles) loads: go out before the prologue.
+__device__ __forceinline__ int producer_preissue(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
+                                                 const CUtensorMap *tmt, const DrArgs &p, int n_units)
+{
+    int n = 0;
+    TileWalk tw;
+    tw.init(n_units, p.n_strips);
+    while (n < kStages && tw.next()) {
+        issue_tile(sm, tmc, tms, tmt, n, tw.rt, tw.st);
+        ++n;
+    }
+    return n;
+}
+
+__device__ __forceinline__ int producer_loop(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
+                                             const CUtensorMap *tmt, const DrArgs &p, int n_units, int pre,
+                                             int e0)
+{
+    int issued = pre;
+    TileWalk tw;
+    tw.init(n_units, p.n_strips);
+    for (int it = 0; tw.next(); ++it) {
+        const int rt = tw.rt, st = tw.st;
+        const int s = it % kStages;
+        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+        if (it >= pre) {
+            const bool ok = mbar_wait_bounded(&sm.empty[s], ph ^ 1u);
+            if (!ok)
+                raise_status(p.status, kDevErrTimeout);
+            if (!ok || sm.abort_flag) {
+                sm.abort_flag = 1;
+                break;
+            }
+            issue_tile(sm, tmc, tms, tmt, s, rt, st);
+            issued = it + 1;
+        }
+        const int e = expert_of_row(sm.offs, p.E, rt * kTileRows);
+        const int off = sm.offs[e];
+        const int n = sm.offs[e + 1] - off;
+        const float se = sm.se_cache[e];
+        const int slot = e - e0 < kSlots ? e - e0 : -1;
+        sm.meta[s] = StageMeta{e, off, n, slot, se, __fdiv_rn(se, 6.0f)};
+        mbar_arrive(&sm.full[s]); // releases the metadata with the stage
+    }
+    return issued;
+}
+
+// Prologue (whole CTA): S_enc of every expert the CTA's tiles belong to, from
+// the 4-byte token amaxes in the row trailers (eight loads in flight per
+// thread, issued before the first tile loads so they do not queue behind
+// them), plus the table S_enc / s over all E4M3 codes s for the first kSlots
+// experts; the CTA holding an expert's first tile of strip 0 also writes the
+// expert's metadata.  Returns the CTA's first expert.
+__device__ __forceinline__ int expert_prologue(DrSmem &sm, const DrArgs &p, int n_units, uint32_t *red,
+                                               const CUtensorMap *tmc, const CUtensorMap *tms,
+                                               const CUtensorMap *tmt, int *pre)
+{
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int lo = (int)(b * n_units / G), hi = (int)((b + 1) * n_units / G);
+    const bool producer = threadIdx.x == kConsumers;
+    if (lo >= hi)
+        return 0;
+    const int e0 = expert_of_row(sm.offs, p.E, (lo / p.n_strips) * kTileRows);
+    const int e1 = expert_of_row(sm.offs, p.E, ((hi - 1) / p.n_strips) * kTileRows);
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int e = e0; e <= e1; ++e) {
+        const int off = sm.offs[e];
+        const int end = min(sm.offs[e + 1], p.R_cap);
+        uint32_t m = 0; // non-negative floats compare as their bit patterns
+        for (int r = off + tid; r < end; r += 8 * nt) {
+            uint32_t v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int rr = r + j * nt;
+                v[j] = rr < end ? __ldg(reinterpret_cast<const uint32_t *>(p.rows + (int64_t)rr * p.S + p.S - 12)) : 0u;
+            }
+            if (producer && e == e0 && r == off + tid)
+                *pre = producer_preissue(sm, tmc, tms, tmt, p, n_units);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                m = max(m, v[j]);
+        }
+        if (producer && e == e0 && off + tid >= end)
+            *pre = producer_preissue(sm, tmc, tms, tmt, p, n_units);
+        m = __reduce_max_sync(0xffffffffu, m);
+        if ((tid & 31) == 0)
+            red[tid >> 5] = m;
+        __syncthreads();
+        m = 0u;
+        for (int w = 0; w < (nt + 31) / 32; ++w)
+            m = max(m, red[w]);
+        const float a = u2f(m), ac = 4.0f * a;
+        const float se = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
+        if (tid == 0) {
+            sm.se_cache[e] = se;
+            const int u_owner = (off / kTileRows) * p.n_strips; // strip 0 of the expert's first tile
+            if (end > off && u_owner >= lo && u_owner < hi) {
+                p.amax_row[e] = a;
+                p.amax_col[e] = ac;
+                p.scale_enc[e] = se;
+            }
+        }
+        if (e - e0 < kSlots && tid < 128) {
+            const float sv = e4m3_to_f32((uint32_t)tid);
+            sm.rtab[e - e0][tid] = (sv == 0.0f) ? 0.0f : __fdiv_rn(se, sv);
+        }
+        __syncthreads();
+    }
+    return e0;
 }
 
 __device__ __forceinline__ void st16g(void *p, uint4 v)
@@ -136,32 +276,99 @@ __device__ __forceinline__ void st16g(void *p, uint4 v)
                  : "memory");
 }
 
+// One 16-row block of the thread's two columns: decode, RHT, block scales,
+// E2M1 codes.  Returns the 8 code bytes of each column (cw0, cw1) and the two
+// E4M3 scale codes (s2: column 0 in the low byte).
 template <bool kSR>
-__device__ __forceinline__ void consumer_loop(DrSmem &sm, const CUtensorMap *tm_rw, const DrArgs &p,
-                                              int n_units)
+__device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 *tab, const float *rtab, int c,
+                                          int r0, float ce, const DrArgs &p, const StageMeta &m, int h0, int rl,
+                                          uint2 &cw0, uint2 &cw1, uint32_t &s2)
 {
-    const int c = threadIdx.x; // 0..127
+    // tab: this column block's decode scales of rows r0 .. r0+15, as (sc, sc)
+    const float4 *tp = reinterpret_cast<const float4 *>(tab);
+    float2 u[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float4 t4 = tp[i >> 1];
+        const float2 qa = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i][c]));
+        const float2 qb = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i + 1][c]));
+        // decoded values are exact products; len = 1 butterflies
+        const float2 da = mul2(qa, make_float2(t4.x, t4.y));
+        const float2 db = mul2(qb, make_float2(t4.z, t4.w));
+        u[i] = add2(da, db);
+        u[i + 1] = sub2(da, db);
+    }
+    // remaining Walsh-Hadamard butterflies, len = 2, 4, 8
+#pragma unroll
+    for (int len = 2; len < 16; len <<= 1) {
+#pragma unroll
+        for (int a = 0; a < 16; ++a) {
+            if (a & len)
+                continue;
+            const float2 x = u[a], y = u[a + len];
+            u[a] = add2(x, y);
+            u[a + len] = sub2(x, y);
+        }
+    }
+    float b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        b0 = fmaxf(b0, fabsf(u[i].x));
+        b1 = fmaxf(b1, fabsf(u[i].y));
+    }
+    s2 = cvt_e4m3x2(b0 * ce, b1 * ce);
+    const float2 r2 = make_float2(rtab[s2 & 0xffu], rtab[(s2 >> 8) & 0xffu]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        u[i] = mul2(u[i], r2);
+    if (kSR) {
+        const uint64_t pos = (uint64_t)m.off * (uint64_t)p.H + (uint64_t)h0 * (uint64_t)m.n + (uint64_t)(rl + r0);
+        const Philox4 ra = sr_bytes16(p.seed, 1u, pos);
+        const Philox4 rb = sr_bytes16(p.seed, 1u, pos + (uint64_t)m.n);
+        const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
+        const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            u[i].x = sr_e2m1_value(u[i].x, (wa[i >> 2] >> (8 * (i & 3))) & 0xffu);
+            u[i].y = sr_e2m1_value(u[i].y, (wb[i >> 2] >> (8 * (i & 3))) & 0xffu);
+        }
+    }
+    cw0 = make_uint2(cvt_e2m1x8(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x),
+                     cvt_e2m1x8(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x));
+    cw1 = make_uint2(cvt_e2m1x8(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y),
+                     cvt_e2m1x8(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y));
+}
+
+template <bool kSR>
+__device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_rw, const DrArgs &p, int n_units)
+{
+    const int c = threadIdx.x;          // 0 .. kConsumers-1
+    const int warp = c >> 5, lane = c & 31;
+    const int hh = warp >> 2;           // rows [64 hh, 64 hh + 64) of the tile
+    const int cq = warp & 3;            // column pairs [32 cq, 32 cq + 32) of the strip
+    const int pc = 32 * cq + lane;      // this thread's column pair
     const int H = p.H;
-    int it = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+    float2(*tab)[kWTabStride] = sm.wtab[warp];
+    int done = 0;
+    TileWalk tw;
+    tw.init(n_units, p.n_strips);
+    for (int it = 0; tw.next(); ++it) {
+        const int rt = tw.rt, st = tw.st;
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-        const int buf = it & 1;
-        bool failed = false;
-        if (!mbar_wait_bounded(&sm.full[s], ph)) {
-            failed = true;
-            sm.abort_flag = 1;
-            raise_status(p.status, kDevErrTimeout);
+        if (!mbar_wait_bounded(&sm.full[s], ph) || sm.abort_flag) {
+            if (lane == 0) {
+                sm.abort_flag = 1;
+                raise_status(p.status, kDevErrTimeout);
+            }
+            break;
         }
-        const int rt = u / p.n_strips, st = u - rt * p.n_strips;
+        const StageMeta m = sm.meta[s];
         const int row0 = rt * kTileRows;
-        const int e = expert_of_row(p.offsets, p.E, row0);
-        const int off_e = __ldg(p.offsets + e);
-        const int n_e = __ldg(p.offsets + e + 1) - off_e;
-        const int rl = row0 - off_e;
+        const int rl = row0 - m.off;
 
         // rowwise operand: codes by TMA store, scales and token scale by threads
-        if (p.do_rowwise && !failed) {
+        if (p.do_rowwise && c < kTileRows) {
             if (c == 0) {
                 tma_store_2d(tm_rw, st * kCodeBytes, row0, &sm.codes[s][0][0]);
                 tma_store_commit();
@@ -179,141 +386,76 @@ __device__ __forceinline__ void consumer_loop(DrSmem &sm, const CUtensorMap *tm_
                 p.rw_row_scale[row0 + c] = u2f(sm.trailer[s][c][0]);
         }
 
-        // per-tile tables: decode scale of (row c, column block cb) with the
-        // RHT sign and the 1/4 folded in (exact), and S_enc / s per E4M3 code
-        {
-            float rs = u2f(sm.trailer[s][c][0]) * 0.25f;
-            if ((p.sign_mask >> (c & 15)) & 1u)
+        // this warp's decode scales: rows 64 hh + {lane, lane + 32}, column
+        // blocks 4 cq .. 4 cq + 3, with the RHT sign and the 1/4 folded in
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int rloc = lane + 32 * h, r = 64 * hh + rloc;
+            float rs = u2f(sm.trailer[s][r][0]) * 0.25f;
+            if ((p.sign_mask >> (r & 15)) & 1u)
                 rs = -rs;
-            const uint32_t *sc4 = reinterpret_cast<const uint32_t *>(&sm.scales[s][c][0]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t w = sc4[q];
-                const float2 a = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w & 0xffffu));
-                const float2 b = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w >> 16));
-                sm.table[buf][4 * q + 0][c] = a.x * rs;
-                sm.table[buf][4 * q + 1][c] = a.y * rs;
-                sm.table[buf][4 * q + 2][c] = b.x * rs;
-                sm.table[buf][4 * q + 3][c] = b.y * rs;
-            }
-            const float se = __ldg(p.scale_enc + e);
-            const float sv = e4m3_to_f32((uint32_t)c);
-            sm.rtab[buf][c] = (sv == 0.0f) ? 0.0f : __fdiv_rn(se, sv);
+            const uint32_t w4 = *reinterpret_cast<const uint32_t *>(&sm.scales[s][r][4 * cq]);
+            const float2 a = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w4 & 0xffffu));
+            const float2 b = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w4 >> 16));
+            const float v0 = a.x * rs, v1 = a.y * rs, v2 = b.x * rs, v3 = b.y * rs;
+            tab[0][rloc] = make_float2(v0, v0);
+            tab[1][rloc] = make_float2(v1, v1);
+            tab[2][rloc] = make_float2(v2, v2);
+            tab[3][rloc] = make_float2(v3, v3);
         }
-        // one decision for all consumers: stop if any wait gave up
-        if (named_bar_or(1, kConsumers, failed || sm.abort_flag != 0))
-            break;
-
-        const float se = __ldg(p.scale_enc + e);
-        const float ce = __fdiv_rn(se, 6.0f);
-        const int h0 = st * kTileCols + 2 * c;
-        if (h0 < H) {
-            const int cb = c >> 3;
-            uint32_t cw0[16], cw1[16];
-            uint32_t sc0[2] = {0u, 0u}, sc1[2] = {0u, 0u};
-#pragma unroll
-            for (int blk = 0; blk < 8; ++blk) {
-                const float4 *tp = reinterpret_cast<const float4 *>(&sm.table[buf][cb][blk * 16]);
-                float scv[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 t4 = tp[q];
-                    scv[4 * q + 0] = t4.x; scv[4 * q + 1] = t4.y;
-                    scv[4 * q + 2] = t4.z; scv[4 * q + 3] = t4.w;
-                }
-                float2 u[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint32_t byte = sm.codes[s][blk * 16 + i][c];
-                    const float2 qv = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(byte));
-                    u[i] = mul2(qv, make_float2(scv[i], scv[i]));
-                }
-                // 16-point Walsh-Hadamard butterflies, len = 1, 2, 4, 8
-#pragma unroll
-                for (int len = 1; len < 16; len <<= 1) {
-#pragma unroll
-                    for (int a = 0; a < 16; ++a) {
-                        if (a & len)
-                            continue;
-                        const float2 x = u[a], y = u[a + len];
-                        u[a] = add2(x, y);
-                        u[a + len] = sub2(x, y);
-                    }
-                }
-                float b0 = 0.0f, b1 = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    b0 = fmaxf(b0, fabsf(u[i].x));
-                    b1 = fmaxf(b1, fabsf(u[i].y));
-                }
-                const uint32_t s2 = cvt_e4m3x2(b0 * ce, b1 * ce);
-                const uint32_t s0 = s2 & 0xffu, s1 = (s2 >> 8) & 0xffu;
-                const float2 r2 = make_float2(sm.rtab[buf][s0], sm.rtab[buf][s1]);
-                sc0[blk >> 2] |= s0 << (8 * (blk & 3));
-                sc1[blk >> 2] |= s1 << (8 * (blk & 3));
-                float2 v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    v[i] = mul2(u[i], r2);
-                if (kSR) {
-                    const uint64_t pos = (uint64_t)off_e * (uint64_t)H + (uint64_t)h0 * (uint64_t)n_e +
-                                         (uint64_t)(rl + blk * 16);
-                    const Philox4 ra = sr_bytes16(p.seed, 1u, pos);
-                    const Philox4 rb = sr_bytes16(p.seed, 1u, pos + (uint64_t)n_e);
-                    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
-                    const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        v[i].x = sr_e2m1_value(v[i].x, (wa[i >> 2] >> (8 * (i & 3))) & 0xffu);
-                        v[i].y = sr_e2m1_value(v[i].y, (wb[i >> 2] >> (8 * (i & 3))) & 0xffu);
-                    }
-                }
-                uint32_t a0 = 0u, a1 = 0u, b0w = 0u, b1w = 0u;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    a0 |= cvt_e2m1x2(v[2 * m].x, v[2 * m + 1].x) << (8 * m);
-                    a1 |= cvt_e2m1x2(v[8 + 2 * m].x, v[8 + 2 * m + 1].x) << (8 * m);
-                    b0w |= cvt_e2m1x2(v[2 * m].y, v[2 * m + 1].y) << (8 * m);
-                    b1w |= cvt_e2m1x2(v[8 + 2 * m].y, v[8 + 2 * m + 1].y) << (8 * m);
-                }
-                cw0[2 * blk] = a0;
-                cw0[2 * blk + 1] = a1;
-                cw1[2 * blk] = b0w;
-                cw1[2 * blk + 1] = b1w;
-            }
-            // columns h0 and h0+1: 64 code bytes and 8 scale bytes each
-            uint8_t *cc = p.cw_codes + (int64_t)off_e * (H / 2) + (int64_t)(rl / 2);
-            uint8_t *cs = p.cw_scales + (int64_t)off_e * (H / 16) + (int64_t)(rl / 16);
-            uint8_t *d0 = cc + (int64_t)h0 * (n_e / 2);
-            uint8_t *d1 = d0 + (n_e / 2);
+        const float *rtab = m.slot >= 0 ? sm.rtab[m.slot] : sm.wrtab[warp];
+        if (m.slot < 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                st16g(d0 + 16 * q, make_uint4(cw0[4 * q], cw0[4 * q + 1], cw0[4 * q + 2], cw0[4 * q + 3]));
-                st16g(d1 + 16 * q, make_uint4(cw1[4 * q], cw1[4 * q + 1], cw1[4 * q + 2], cw1[4 * q + 3]));
+                const int code = lane + 32 * q;
+                const float sv = e4m3_to_f32((uint32_t)code);
+                sm.wrtab[warp][code] = (sv == 0.0f) ? 0.0f : __fdiv_rn(m.se, sv);
             }
-            *reinterpret_cast<uint2 *>(cs + (int64_t)h0 * (n_e / 16)) = make_uint2(sc0[0], sc0[1]);
-            *reinterpret_cast<uint2 *>(cs + (int64_t)(h0 + 1) * (n_e / 16)) = make_uint2(sc1[0], sc1[1]);
+        }
+        __syncwarp();
+
+        const int h0 = st * kTileCols + 2 * pc;
+        if (h0 < H) {
+            const float2 *ctab = &tab[lane >> 3][0];
+            uint8_t *d0 = p.cw_codes + (int64_t)m.off * (H / 2) + (int64_t)h0 * (m.n / 2) + (rl + 64 * hh) / 2;
+            uint8_t *d1 = d0 + (m.n / 2);
+            uint32_t sc0 = 0u, sc1 = 0u;
+#pragma unroll 1
+            for (int bp = 0; bp < 2; ++bp) {
+                uint2 a0, a1, b0, b1;
+                uint32_t s2a, s2b;
+                const int r0 = 64 * hh + 32 * bp;
+                rht_block<kSR>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, p, m, h0, rl, a0, a1, s2a);
+                rht_block<kSR>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, p, m, h0, rl, b0, b1, s2b);
+                st16g(d0 + 16 * bp, make_uint4(a0.x, a0.y, b0.x, b0.y));
+                st16g(d1 + 16 * bp, make_uint4(a1.x, a1.y, b1.x, b1.y));
+                sc0 |= ((s2a & 0xffu) | ((s2b & 0xffu) << 8)) << (16 * bp);
+                sc1 |= (((s2a >> 8) & 0xffu) | (((s2b >> 8) & 0xffu) << 8)) << (16 * bp);
+            }
+            uint8_t *cs = p.cw_scales + (int64_t)m.off * (H / 16) + (int64_t)h0 * (m.n / 16) + (rl + 64 * hh) / 16;
+            *reinterpret_cast<uint32_t *>(cs) = sc0;
+            *reinterpret_cast<uint32_t *>(cs + m.n / 16) = sc1;
         }
 
         // release the stage (after the rowwise TMA store has read it)
         if (c == 0 && p.do_rowwise)
             tma_store_wait_read0();
         __syncwarp();
-        if ((c & 31) == 0)
+        if (lane == 0)
             mbar_arrive(&sm.empty[s]);
+        done = it + 1;
     }
-    if (c == 0) {
-        sm.consumed = it;
-        if (p.do_rowwise)
-            tma_store_wait0();
-    }
+    if (c == 0 && p.do_rowwise)
+        tma_store_wait0();
+    return done;
 }
 
+template <bool kSR>
 __global__ void __launch_bounds__(kThreads, 2)
 direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
                       const __grid_constant__ CUtensorMap tm_scales,
                       const __grid_constant__ CUtensorMap tm_trailer,
-                      const __grid_constant__ CUtensorMap tm_rw, DrArgs p, int sr)
+                      const __grid_constant__ CUtensorMap tm_rw, DrArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
     DrSmem &sm = *reinterpret_cast<DrSmem *>(
@@ -322,13 +464,13 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], kConsumers / 32);
+            mbar_init(&sm.empty[i], kConsumerWarps);
         }
         sm.abort_flag = 0;
         sm.consumed = 0;
         fence_mbar_init();
     }
-    if (warp == kConsumers / 32 && lane == 0) {
+    if (warp == kConsumerWarps && lane == 0) {
         tma_prefetch_desc(&tm_codes);
         tma_prefetch_desc(&tm_scales);
         tma_prefetch_desc(&tm_trailer);
@@ -337,7 +479,10 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     pdl_launch_dependents();
     pdl_wait();
 
-    int R = __ldg(p.offsets + p.E);
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x)
+        sm.offs[i] = __ldg(p.offsets + i);
+    __syncthreads();
+    int R = sm.offs[p.E];
     if (R > p.R_cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0)
             raise_status(p.status, kDevErrCapacity);
@@ -345,34 +490,34 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
     const int n_units = (R / kTileRows) * p.n_strips;
 
+    __shared__ uint32_t red[kThreads / 32];
+    int pre = 0;
+    const int e0 = expert_prologue(sm, p, n_units, red, &tm_codes, &tm_scales, &tm_trailer, &pre);
+
     int issued = 0;
-    if (warp == kConsumers / 32) {
-        if (lane == 0) {
-            for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++issued) {
-                const int s = issued % kStages;
-                const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
-                if (!mbar_wait_bounded(&sm.empty[s], ph ^ 1u)) {
-                    sm.abort_flag = 1;
-                    raise_status(p.status, kDevErrTimeout);
-                    break;
+    if (warp == kConsumerWarps) {
+        if (lane == 0)
+            issued = producer_loop(sm, &tm_codes, &tm_scales, &tm_trailer, p, n_units, pre, e0);
+        // metadata of the experts that own no rows
+        if (blockIdx.x == 0) {
+            for (int e = lane; e < p.E; e += 32) {
+                if (__ldg(p.offsets + e + 1) == __ldg(p.offsets + e)) {
+                    p.amax_row[e] = 0.0f;
+                    p.amax_col[e] = 0.0f;
+                    p.scale_enc[e] = 1.0f;
                 }
-                if (sm.abort_flag)
-                    break;
-                const int rt = u / p.n_strips, st = u - rt * p.n_strips;
-                mbar_arrive_expect_tx(&sm.full[s], kStageTx);
-                tma_load_2d(&sm.codes[s][0][0], &tm_codes, st * kCodeBytes, rt * kTileRows, &sm.full[s]);
-                tma_load_2d(&sm.scales[s][0][0], &tm_scales, st * kScaleBytes, rt * kTileRows, &sm.full[s]);
-                tma_load_2d(&sm.trailer[s][0][0], &tm_trailer, 0, rt * kTileRows, &sm.full[s]);
             }
         }
-    } else if (sr) {
-        consumer_loop<true>(sm, &tm_rw, p, n_units);
     } else {
-        consumer_loop<false>(sm, &tm_rw, p, n_units);
+        const int done = consumer_loop<kSR>(sm, &tm_rw, p, n_units);
+        if (threadIdx.x == 0)
+            sm.consumed = done;
     }
     __syncthreads();
+    // after an abort warps may have consumed different numbers of tiles
+    
     // never leave with a tile load still in flight (only after an abort)
-    if (warp == kConsumers / 32 && lane == 0) {
+    if (warp == kConsumerWarps && lane == 0) {
         for (int i = sm.consumed; i < issued; ++i)
             (void)mbar_wait_bounded(&sm.full[i % kStages], (uint32_t)(i / kStages) & 1u);
     }
@@ -385,8 +530,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     if (!fn) {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     }
@@ -405,8 +550,26 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Empty-expert metadata when no tile kernel runs (R_cap < one tile).
+__global__ void small_meta_kernel(const uint8_t *rows, int64_t S, const int32_t *offsets, int E, int R_cap,
+                                  float *amax_row, float *amax_col, float *scale_enc)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        uint32_t m = 0;
+        const int hi = min(offsets[e + 1], R_cap);
+        for (int r = offsets[e]; r < hi; ++r)
+            m = max(m, *reinterpret_cast<const uint32_t *>(rows + (int64_t)r * S + S - 12));
+        const float a = u2f(m), ac = 4.0f * a;
+        amax_row[e] = a;
+        amax_col[e] = ac;
+        scale_enc[e] = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
+    }
 }
 
 cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
@@ -415,10 +578,9 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
                                   uint32_t *status)
 {
     const int64_t S = row_bytes(H);
-    cudaError_t err = launch_pdl(expert_amax_kernel, dim3(E), dim3(256), 0, c.stream, rows, R_cap, S,
-                                 offsets, E, out.amax_row, out.amax_col, out.scale_enc, status);
-    if (err != cudaSuccess || R_cap < kTileRows)
-        return err;
+    if (R_cap < kTileRows)
+        return launch_pdl(small_meta_kernel, dim3(1), dim3(256), 0, c.stream, rows, S, offsets, E, R_cap,
+                          out.amax_row, out.amax_col, out.scale_enc);
 
     CUtensorMap tm_codes, tm_scales, tm_trailer, tm_rw;
     memset(&tm_rw, 0, sizeof(tm_rw));
@@ -432,6 +594,8 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
         return cudaErrorInvalidValue;
 
     DrArgs a;
+    a.rows = rows;
+    a.S = S;
     a.offsets = offsets;
     a.E = E;
     a.H = H;
@@ -441,6 +605,8 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     a.rw_row_scale = out.rw_row_scale;
     a.cw_codes = out.cw_codes;
     a.cw_scales = out.cw_scales;
+    a.amax_row = out.amax_row;
+    a.amax_col = out.amax_col;
     a.scale_enc = out.scale_enc;
     a.seed = seed;
     a.sign_mask = sign_mask;
@@ -448,8 +614,9 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     a.do_rowwise = do_rw;
 
     const size_t smem = sizeof(DrSmem) + 1024;
-    static int done[2] = {0, 0};
-    err = ensure_smem_limit(direct_receive_kernel, c.device, (int)smem, done);
+    static int done_rn[2] = {0, 0}, done_sr[2] = {0, 0};
+    cudaError_t err = rounding == 1 ? ensure_smem_limit(direct_receive_kernel<true>, c.device, (int)smem, done_sr)
+                                    : ensure_smem_limit(direct_receive_kernel<false>, c.device, (int)smem, done_rn);
     if (err != cudaSuccess)
         return err;
     const int64_t max_units = (int64_t)(R_cap / kTileRows) * a.n_strips;
@@ -458,8 +625,11 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
         grid = max_units;
     if (grid < 1)
         grid = 1;
-    return launch_pdl(direct_receive_kernel, dim3((unsigned)grid), dim3(kThreads), smem, c.stream, tm_codes,
-                      tm_scales, tm_trailer, tm_rw, a, rounding == 1 ? 1 : 0);
+    if (rounding == 1)
+        return launch_pdl(direct_receive_kernel<true>, dim3((unsigned)grid), dim3(kThreads), smem, c.stream,
+                          tm_codes, tm_scales, tm_trailer, tm_rw, a);
+    return launch_pdl(direct_receive_kernel<false>, dim3((unsigned)grid), dim3(kThreads), smem, c.stream, tm_codes,
+                      tm_scales, tm_trailer, tm_rw, a);
 }
 
 } // namespace epq

@@ -4,101 +4,30 @@
 // (description: expert-major received rows returned as a per-expert grouped
 // tensor; review thread: each expert slot aligned to a multiple of 128 rows).
 //
-// Two kernels, both over chunks of 512 tokens (one thread per token):
-//  1. route_count: validate ids, build per-expert token bitmasks of the chunk
-//     (each warp owns one 32-bit word of every expert's mask, filled with
-//     __match_any_sync so no atomics are needed), write the chunk's
-//     per-expert histogram and each slot's stable rank inside the chunk.
-//  2. route_assign: every chunk sums the histograms of the chunks before it
-//     (its base inside each expert) and of all chunks (the totals), scans
-//     the aligned totals into expert offsets, and rewrites its slots' ranks
-//     into global row indices.  Rows of an expert follow ascending token
-//     order because chunks and ranks are both in token order.
+// One cooperative launch (every CTA resident), two phases around one grid
+// barrier:
+//  1. each CTA takes a contiguous run of 512-token chunks (one thread per
+//     token), validates the ids and ranks every slot among the CTA's earlier
+//     slots of the same expert: per chunk, each warp owns one 32-bit word of
+//     every expert's token mask (filled with __match_any_sync, no atomics),
+//     the words are prefix-counted, and a running per-expert count carries
+//     over to the next chunk; the CTA's per-expert totals go to the workspace.
+//  2. after the barrier every CTA sums the totals of the CTAs before it (its
+//     base inside each expert) and of all CTAs, scans the aligned totals into
+//     expert offsets and turns its slots' ranks into row indices.  Rows of an
+//     expert follow ascending token order because CTAs, chunks and ranks are
+//     all in token order.
+// The barrier waits are bounded: on timeout EP_DEV_ERR_TIMEOUT is raised and
+// the outputs are invalid.
 #include "epq_device.cuh"
 #include "epq_internal.h"
 
 namespace epq {
 
-constexpr int kChunk = 512;              // tokens per CTA
+constexpr int kChunk = 512;              // tokens per chunk, one thread each
 constexpr int kWords = kChunk / 32;      // mask words per expert
-constexpr int kRankBits = 10;            // temp encoding: expert << 10 | rank
-
-__global__ void __launch_bounds__(kChunk)
-route_count_kernel(const int32_t *__restrict__ topk, int T, int k, int E,
-                   int32_t *__restrict__ hist, int32_t *__restrict__ dest,
-                   uint32_t *__restrict__ status)
-{
-    extern __shared__ uint32_t sm[];
-    uint32_t *mask = sm;                       // [E][kWords]
-    uint32_t *pre = sm + (size_t)E * kWords;   // [E][kWords]
-    pdl_launch_dependents();
-    pdl_wait();
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int chunk = blockIdx.x;
-    const int64_t t = (int64_t)chunk * kChunk + tid;
-    for (int i = tid; i < E * kWords; i += kChunk)
-        mask[i] = 0u;
-    __syncthreads();
-
-    uint32_t bad = 0;
-    for (int j = 0; j < k; ++j) {
-        int e = -1;
-        if (t < T) {
-            const int v = topk[t * k + j];
-            if (v != -1) {
-                if (v < 0 || v >= E) {
-                    bad |= kDevErrBadExpert;
-                } else {
-                    bool dup = false;
-                    for (int jj = 0; jj < j; ++jj)
-                        dup |= (topk[t * k + jj] == v);
-                    if (dup)
-                        bad |= kDevErrDupExpert;
-                    else
-                        e = v;
-                }
-            }
-            dest[t * k + j] = e; // validated expert id, consumed below
-        }
-        // lanes routed to the same expert in this slot: their bits of word
-        // `warp` of that expert's mask; the lowest such lane writes them
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0u)
-            mask[e * kWords + warp] |= peers;
-    }
-    if (bad)
-        raise_status(status, bad);
-    __syncthreads();
-
-    // exclusive prefix over the chunk's words of every expert, and totals
-    for (int e = warp; e < E; e += kChunk / 32) {
-        const uint32_t c = (lane < kWords) ? __popc(mask[e * kWords + lane]) : 0u;
-        uint32_t x = c;
-#pragma unroll
-        for (int o = 1; o < kWords; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o)
-                x += y;
-        }
-        if (lane < kWords)
-            pre[e * kWords + lane] = x - c;
-        if (lane == kWords - 1)
-            hist[(int64_t)chunk * E + e] = (int32_t)x;
-    }
-    __syncthreads();
-
-    if (t < T) {
-        for (int j = 0; j < k; ++j) {
-            const int e = dest[t * k + j];
-            if (e >= 0) {
-                const uint32_t below = mask[e * kWords + warp] & ((1u << lane) - 1u);
-                const int rank = (int)(pre[e * kWords + warp] + __popc(below));
-                dest[t * k + j] = (e << kRankBits) | rank;
-            }
-        }
-    }
-}
+constexpr int kRankBits = 21;            // temp encoding: expert << 21 | rank in CTA
+constexpr int kWsHeader = 4;             // workspace words before the totals: barrier count, generation
 
 // In-place exclusive scan of a[0, n) in shared memory (n <= 1024); every thread
 // of the block calls it; returns the total.
@@ -143,44 +72,145 @@ __device__ int block_exclusive_scan(int *a, int n, int *wtmp)
     return total;
 }
 
-__global__ void __launch_bounds__(kChunk)
-route_assign_kernel(int T, int k, int E, int A, int nchunks, const int32_t *__restrict__ hist,
-                    int32_t *__restrict__ offsets, int32_t *__restrict__ counts,
-                    int32_t *__restrict__ dest)
+// Grid-wide barrier over a cooperative launch.  Self-resetting: the last CTA
+// to arrive zeroes the count and bumps the generation the others wait on, so
+// the two workspace words are back to a usable state after every call (they
+// must be zero before the first call).  Bounded: gives up after ~1 s.
+__device__ bool grid_barrier(uint32_t *count, uint32_t *gen, uint32_t n, int *flag)
 {
-    __shared__ int base[1024];
-    __shared__ int off[1024];
-    __shared__ int cnt[1024];
-    __shared__ int wtmp[32];
-    pdl_launch_dependents();
-    pdl_wait();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const uint32_t g = ld_acquire_gpu(gen);
+        __threadfence();
+        const uint32_t arrived = atomicAdd(count, 1u) + 1u;
+        if (arrived == n) {
+            atomicExch(count, 0u);
+            __threadfence();
+            atomicAdd(gen, 1u);
+        } else {
+            ok = 0;
+            for (uint32_t i = 0; i < (1u << 23); ++i) {
+                if (ld_acquire_gpu(gen) != g) {
+                    ok = 1;
+                    break;
+                }
+                if (i > 4096)
+                    __nanosleep(128);
+            }
+        }
+        __threadfence();
+        *flag = ok;
+    }
+    __syncthreads();
+    return *flag != 0;
+}
 
-    const int tid = threadIdx.x, chunk = blockIdx.x;
+// Fast path: one 512-token chunk per CTA and k <= 8: the validated ids and
+// the ranks of a thread's slots stay in registers between the phases.
+constexpr int kRegSlots = 8;
+
+__global__ void __launch_bounds__(kChunk)
+route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A,
+                      int32_t *__restrict__ offsets, int32_t *__restrict__ counts, int32_t *__restrict__ dest,
+                      uint32_t *__restrict__ ws, uint32_t *__restrict__ status)
+{
+    extern __shared__ uint32_t sm[];
+    uint32_t *mask = sm;                         // [E][kWords]
+    uint32_t *pre = mask + (size_t)E * kWords;   // [E][kWords]
+    int *tot = reinterpret_cast<int *>(pre + (size_t)E * kWords);  // [E]
+    int *base = tot + E;                         // [E]
+    int *off = base + E;                         // [E]
+    __shared__ int wtmp[32];
+    __shared__ int flag;
+
+    // the next kernel may be scheduled now: it waits for this grid's
+    // completion (griddepcontrol.wait) before it reads anything
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cta = blockIdx.x, nctas = gridDim.x;
+    int32_t *hist = reinterpret_cast<int32_t *>(ws + kWsHeader);   // [nctas][E]
+    const int64_t t = (int64_t)cta * kChunk + tid;
+
+    int raw[kRegSlots], ev[kRegSlots], rk[kRegSlots];
+#pragma unroll
+    for (int j = 0; j < kRegSlots; ++j)
+        raw[j] = (t < T && j < k) ? topk[t * k + j] : -1;
+    for (int i = tid; i < E * kWords; i += kChunk)
+        mask[i] = 0u;
+    __syncthreads();
+
+    uint32_t bad = 0;
+#pragma unroll
+    for (int j = 0; j < kRegSlots; ++j) {
+        int e = -1;
+        const int v = raw[j];
+        if (j < k && v != -1) {
+            if (v < 0 || v >= E) {
+                bad |= kDevErrBadExpert;
+            } else {
+                bool dup = false;
+#pragma unroll
+                for (int jj = 0; jj < j; ++jj)
+                    dup |= (raw[jj] == v);
+                if (dup)
+                    bad |= kDevErrDupExpert;
+                else
+                    e = v;
+            }
+        }
+        ev[j] = e;
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0u)
+            mask[e * kWords + warp] |= peers;
+    }
+    if (bad)
+        raise_status(status, bad);
+    __syncthreads();
+    for (int e = warp; e < E; e += kChunk / 32) {
+        const uint32_t c = (lane < kWords) ? __popc(mask[e * kWords + lane]) : 0u;
+        uint32_t x = c;
+#pragma unroll
+        for (int o = 1; o < kWords; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
+        }
+        if (lane < kWords)
+            pre[e * kWords + lane] = x - c;
+        if (lane == kWords - 1)
+            hist[(int64_t)cta * E + e] = (int)x;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRegSlots; ++j) {
+        const int e = ev[j];
+        rk[j] = e >= 0 ? (int)(pre[e * kWords + warp] + __popc(mask[e * kWords + warp] & ((1u << lane) - 1u))) : 0;
+    }
+
+    if (!grid_barrier(ws, ws + 1, (uint32_t)nctas, &flag)) {
+        if (tid == 0)
+            raise_status(status, kDevErrTimeout);
+        return;
+    }
+
     for (int e = tid; e < E; e += kChunk) {
-        int pre = 0, tot = 0;
-        int c = 0;
-        for (; c + 4 <= nchunks; c += 4) {
-            const int h0 = hist[(int64_t)(c + 0) * E + e], h1 = hist[(int64_t)(c + 1) * E + e];
-            const int h2 = hist[(int64_t)(c + 2) * E + e], h3 = hist[(int64_t)(c + 3) * E + e];
-            pre += (c + 0 < chunk ? h0 : 0) + (c + 1 < chunk ? h1 : 0) + (c + 2 < chunk ? h2 : 0) +
-                   (c + 3 < chunk ? h3 : 0);
-            tot += h0 + h1 + h2 + h3;
+        int p = 0, all = 0;
+        for (int c = 0; c < nctas; ++c) {
+            const int h = __ldcg(hist + (int64_t)c * E + e);
+            p += (c < cta) ? h : 0;
+            all += h;
         }
-        for (; c < nchunks; ++c) {
-            const int h = hist[(int64_t)c * E + e];
-            pre += (c < chunk) ? h : 0;
-            tot += h;
-        }
-        base[e] = pre;
-        cnt[e] = tot;
-        off[e] = (tot + A - 1) / A * A;
+        base[e] = p;
+        tot[e] = all;
+        off[e] = (all + A - 1) / A * A;
     }
     __syncthreads();
     const int total = block_exclusive_scan(off, E, wtmp);
-    if (chunk == 0) {
+    if (cta == 0) {
         for (int e = tid; e < E; e += kChunk) {
             offsets[e] = off[e];
-            counts[e] = cnt[e];
+            counts[e] = tot[e];
         }
         if (tid == 0)
             offsets[E] = total;
@@ -188,9 +218,138 @@ route_assign_kernel(int T, int k, int E, int A, int nchunks, const int32_t *__re
     for (int e = tid; e < E; e += kChunk)
         base[e] += off[e];
     __syncthreads();
-
-    const int64_t t = (int64_t)chunk * kChunk + tid;
     if (t < T) {
+#pragma unroll
+        for (int j = 0; j < kRegSlots; ++j)
+            if (j < k)
+                dest[t * k + j] = ev[j] >= 0 ? base[ev[j]] + rk[j] : -1;
+    }
+}
+
+__global__ void __launch_bounds__(kChunk)
+route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, int chunks_per_cta,
+                  int32_t *__restrict__ offsets, int32_t *__restrict__ counts, int32_t *__restrict__ dest,
+                  uint32_t *__restrict__ ws, uint32_t *__restrict__ status)
+{
+    extern __shared__ uint32_t sm[];
+    uint32_t *mask = sm;                         // [E][kWords]
+    uint32_t *pre = mask + (size_t)E * kWords;   // [E][kWords]
+    int *run = reinterpret_cast<int *>(pre + (size_t)E * kWords);  // [E]
+    int *base = run + E;                         // [E]
+    int *off = base + E;                         // [E]
+    __shared__ int wtmp[32];
+    __shared__ int flag;
+
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cta = blockIdx.x, nctas = gridDim.x;
+    int32_t *hist = reinterpret_cast<int32_t *>(ws + kWsHeader);   // [nctas][E]
+    for (int e = tid; e < E; e += kChunk)
+        run[e] = 0;
+
+    // ---- phase 1: ranks inside the CTA's run of chunks
+    uint32_t bad = 0;
+    for (int ch = 0; ch < chunks_per_cta; ++ch) {
+        const int64_t t = ((int64_t)cta * chunks_per_cta + ch) * kChunk + tid;
+        for (int i = tid; i < E * kWords; i += kChunk)
+            mask[i] = 0u;
+        __syncthreads();
+        for (int j = 0; j < k; ++j) {
+            int e = -1;
+            if (t < T) {
+                const int v = topk[t * k + j];
+                if (v != -1) {
+                    if (v < 0 || v >= E) {
+                        bad |= kDevErrBadExpert;
+                    } else {
+                        bool dup = false;
+                        for (int jj = 0; jj < j; ++jj)
+                            dup |= (topk[t * k + jj] == v);
+                        if (dup)
+                            bad |= kDevErrDupExpert;
+                        else
+                            e = v;
+                    }
+                }
+                dest[t * k + j] = e; // validated expert id, consumed below
+            }
+            // lanes routed to the same expert in this slot own their bits of
+            // word `warp` of that expert's mask; the lowest such lane writes them
+            const uint32_t peers = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0u)
+                mask[e * kWords + warp] |= peers;
+        }
+        __syncthreads();
+        // exclusive prefix over the chunk's words of every expert (+ the run)
+        for (int e = warp; e < E; e += kChunk / 32) {
+            const uint32_t c = (lane < kWords) ? __popc(mask[e * kWords + lane]) : 0u;
+            uint32_t x = c;
+#pragma unroll
+            for (int o = 1; o < kWords; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o)
+                    x += y;
+            }
+            const int r0 = run[e];
+            if (lane < kWords)
+                pre[e * kWords + lane] = (uint32_t)r0 + x - c;
+            __syncwarp();
+            if (lane == kWords - 1)
+                run[e] = r0 + (int)x;
+        }
+        __syncthreads();
+        if (t < T) {
+            for (int j = 0; j < k; ++j) {
+                const int e = dest[t * k + j];
+                if (e >= 0) {
+                    const uint32_t below = mask[e * kWords + warp] & ((1u << lane) - 1u);
+                    const int rank = (int)(pre[e * kWords + warp] + __popc(below));
+                    dest[t * k + j] = (e << kRankBits) | rank;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (bad)
+        raise_status(status, bad);
+    for (int e = tid; e < E; e += kChunk)
+        hist[(int64_t)cta * E + e] = run[e];
+
+    if (!grid_barrier(ws, ws + 1, (uint32_t)nctas, &flag)) {
+        if (tid == 0)
+            raise_status(status, kDevErrTimeout);
+        return;
+    }
+
+    // ---- phase 2: offsets, and global rows of this CTA's slots
+    for (int e = tid; e < E; e += kChunk) {
+        int p = 0, tot = 0;
+        for (int c = 0; c < nctas; ++c) {
+            const int h = __ldcg(hist + (int64_t)c * E + e);
+            p += (c < cta) ? h : 0;
+            tot += h;
+        }
+        base[e] = p;
+        run[e] = tot;
+        off[e] = (tot + A - 1) / A * A;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan(off, E, wtmp);
+    if (cta == 0) {
+        for (int e = tid; e < E; e += kChunk) {
+            offsets[e] = off[e];
+            counts[e] = run[e];
+        }
+        if (tid == 0)
+            offsets[E] = total;
+    }
+    for (int e = tid; e < E; e += kChunk)
+        base[e] += off[e];
+    __syncthreads();
+    for (int ch = 0; ch < chunks_per_cta; ++ch) {
+        const int64_t t = ((int64_t)cta * chunks_per_cta + ch) * kChunk + tid;
+        if (t >= T)
+            break;
         for (int j = 0; j < k; ++j) {
             const int v = dest[t * k + j];
             if (v >= 0)
@@ -201,31 +360,51 @@ route_assign_kernel(int T, int k, int E, int A, int nchunks, const int32_t *__re
 
 size_t route_workspace_bytes(int64_t T, int E)
 {
+    // header + per-CTA totals for at most one CTA per 512-token chunk
     const int64_t nch = (T + kChunk - 1) / kChunk;
-    const size_t b = (size_t)nch * (size_t)E * 4u;
-    return b < 16 ? 16 : b;
+    return (size_t)kWsHeader * 4u + (size_t)(nch > 0 ? nch : 1) * (size_t)E * 4u;
 }
 
 cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, int k, int E, int A,
                               int32_t *offsets, int32_t *counts, int32_t *dest, int32_t *hist,
                               uint32_t *status)
 {
+    const size_t smem = (size_t)E * kWords * 4u * 2u + (size_t)E * 4u * 3u;
+    static int done[2] = {0, 0}, done_reg[2] = {0, 0};
+    cudaError_t err = ensure_smem_limit(route_plan_kernel, c.device, 1024 * kWords * 8 + 1024 * 12, done);
+    if (err == cudaSuccess)
+        err = ensure_smem_limit(route_plan_reg_kernel, c.device, 1024 * kWords * 8 + 1024 * 12, done_reg);
+    if (err != cudaSuccess)
+        return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_plan_kernel, kChunk, smem);
+    if (err != cudaSuccess)
+        return err;
+    if (per_sm < 1)
+        return cudaErrorInvalidConfiguration;
     const int nch = (T + kChunk - 1) / kChunk;
-    const size_t smem = (size_t)E * kWords * 4u * 2u;
-    cudaError_t err;
-    if (nch > 0) {
-        // the largest request (E = 1024) is set once per device
-        static int done[2] = {0, 0};
-        err = ensure_smem_limit(route_count_kernel, c.device, 1024 * kWords * 4 * 2, done);
-        if (err != cudaSuccess)
-            return err;
-        err = launch_pdl(route_count_kernel, dim3(nch), dim3(kChunk), smem, c.stream, topk, T, k, E,
-                         hist, dest, status);
-        if (err != cudaSuccess)
-            return err;
+    const int max_ctas = per_sm * c.num_sms;
+    int nctas = nch < 1 ? 1 : nch;
+    int cpc = 1;
+    if (nctas > max_ctas) {
+        cpc = (nch + max_ctas - 1) / max_ctas;
+        nctas = (nch + cpc - 1) / cpc;
     }
-    return launch_pdl(route_assign_kernel, dim3(nch > 0 ? nch : 1), dim3(kChunk), 0, c.stream, T, k,
-                      E, A, nch, (const int32_t *)hist, offsets, counts, dest);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nctas);
+    cfg.blockDim = dim3(kChunk);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cpc == 1 && k <= kRegSlots)
+        return cudaLaunchKernelEx(&cfg, route_plan_reg_kernel, topk, T, k, E, A, offsets, counts, dest,
+                                  reinterpret_cast<uint32_t *>(hist), status);
+    return cudaLaunchKernelEx(&cfg, route_plan_kernel, topk, T, k, E, A, cpc, offsets, counts, dest,
+                              reinterpret_cast<uint32_t *>(hist), status);
 }
 
 } // namespace epq

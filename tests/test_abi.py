@@ -41,7 +41,7 @@ def test_size_helpers():
         assert L.ep_nvfp4_row_bytes(H) % 16 == 0
     assert L.ep_rows_capacity(4096, 2, 16, 128) == 4096 * 2 + 16 * 127
     assert L.ep_route_workspace_bytes(0, 2, 16) >= 16
-    assert L.ep_route_workspace_bytes(16384, 8, 256) == 32 * 256 * 4
+    assert L.ep_route_workspace_bytes(16384, 8, 256) == 16 + 32 * 256 * 4
 
 
 def test_status_strings():

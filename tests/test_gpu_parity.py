@@ -178,7 +178,7 @@ def test_cuda_graph_capture_matches_eager():
     topk = torch.from_numpy(w.topk).cuda()
     R_cap = eager.R_cap
     plan = nq.ep_route_plan(topk, w.E, w.A, R_cap=R_cap)      # warm-up call, allocates outputs
-    ws = torch.empty(nq.lib().ep_route_workspace_bytes(w.T, w.k, w.E) // 4 + 1, dtype=torch.int32, device="cuda")
+    ws = nq.new_route_workspace(w.T, w.k, w.E, "cuda")
     rows = torch.empty((R_cap, nq.row_bytes(w.H)), dtype=torch.uint8, device="cuda")
     out = nq.alloc_grouped(R_cap, w.H, w.E, "cuda")
     torch.cuda.synchronize()
@@ -217,3 +217,19 @@ def test_device_guard_follows_input_device():
     g = GpuRun(w)
     assert g.status == 0
     assert torch.cuda.current_device() == 0
+
+
+@pytest.mark.parametrize("T,E,k", [(3000, 32, 12), (400000, 64, 2), (20000, 1024, 3)])
+def test_route_plan_general_paths(T, E, k):
+    """Routing alone on shapes that leave the register fast path: k > 8, and
+    more 512-token chunks than resident CTAs (several chunks per CTA)."""
+    rng = np.random.default_rng(T + k)
+    topk = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    topk[rng.random((T, k)) < 0.02] = -1
+    off, cnt, dest, st = oracle.route_plan(topk, E, 128)
+    plan = nq.ep_route_plan(torch.from_numpy(topk).cuda(), E, 128)
+    torch.cuda.synchronize()
+    assert_bytes_equal(plan.offsets.cpu().numpy(), off, "offsets")
+    assert_bytes_equal(plan.counts.cpu().numpy(), cnt, "counts")
+    assert_bytes_equal(plan.dest.cpu().numpy()[: T * k], dest, "dest")
+    assert int(plan.status.item()) == st == 0
