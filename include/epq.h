@@ -115,6 +115,39 @@ ep_status ep_route_plan(const int32_t *topk_idx, int64_t T, int k, int E, int A,
                         int32_t *expert_counts, int32_t *dest, void *workspace,
                         size_t ws_bytes, uint32_t *dev_status, void *stream);
 
+/* Size of the scratch array inside the library that ep_route_plan_noalloc
+ * uses in place of a caller's workspace. */
+#define EP_ROUTE_STATIC_SCRATCH_BYTES 262144
+
+/*
+ * ep_route_plan_noalloc -- ep_route_plan without a workspace argument.
+ * The pages have no counterpart: this is a library convenience.  It is for
+ * callers that cannot allocate device memory for a workspace: a runtime or
+ * plugin host that owns the whole GPU's memory in its own pool and passes an
+ * extension only its inputs and outputs, or a latency-critical loop where a
+ * cudaMalloc would synchronise the device.
+ *   Arguments, outputs and device status: as ep_route_plan.  Results are
+ *   identical to ep_route_plan's for the same inputs.
+ *   Limit: ep_route_workspace_bytes(T, k, E) must not exceed
+ *   EP_ROUTE_STATIC_SCRATCH_BYTES (256 KiB: e.g. T <= 131072 tokens at
+ *   E = 256); larger problems return EP_ERR_CAPACITY and launch nothing.
+ *   Memory: allocates nothing, on any call.  The scratch is a fixed device
+ *   array of EP_ROUTE_STATIC_SCRATCH_BYTES that every GPU which loads the
+ *   library holds until the process exits.  The first call on a device looks
+ *   up that device's scratch address (cudaGetSymbolAddress); make that first
+ *   call before any stream capture on the device.  Each call clears the
+ *   scratch's barrier words on `stream` before its kernel.
+ *   Concurrency: all calls on a device share one scratch array, so calls
+ *   whose work may overlap on the GPU (different streams, or several host
+ *   threads) race and give wrong plans; order them on one stream, or use
+ *   ep_route_plan with a workspace per stream.
+ */
+ep_status ep_route_plan_noalloc(const int32_t *topk_idx, int64_t T, int k,
+                                int E, int A, int64_t R_cap,
+                                int32_t *expert_offsets,
+                                int32_t *expert_counts, int32_t *dest,
+                                uint32_t *dev_status, void *stream);
+
 /*
  * ep_nvfp4_pack -- quantise each BF16 token once into a packed NVFP4 row and
  * write that row to each of its destinations; fill padding rows.

@@ -23,11 +23,12 @@ EP_DEV_ERR_BAD_EXPERT = 1
 EP_DEV_ERR_DUP_EXPERT = 2
 EP_DEV_ERR_TIMEOUT = 4
 EP_DEV_ERR_CAPACITY = 8
+EP_ROUTE_STATIC_SCRATCH_BYTES = 262144   # mirrors the macro in include/epq.h
 
 # every symbol include/epq.h declares
 SYMBOLS = ("ep_nvfp4_row_bytes", "ep_rows_capacity", "ep_route_workspace_bytes", "ep_route_plan",
-           "ep_nvfp4_pack", "ep_nvfp4_unpack", "ep_nvfp4_direct_receive", "ep_mxfp8_pack",
-           "ep_status_string")
+           "ep_route_plan_noalloc", "ep_nvfp4_pack", "ep_nvfp4_unpack", "ep_nvfp4_direct_receive",
+           "ep_mxfp8_pack", "ep_status_string")
 
 
 class EpGrouped(ctypes.Structure):
@@ -52,6 +53,8 @@ def _declare(L):
     L.ep_route_workspace_bytes.argtypes = [_I64, _I32, _I32]; L.ep_route_workspace_bytes.restype = ctypes.c_size_t
     L.ep_route_plan.argtypes = [_P, _I64, _I32, _I32, _I32, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
     L.ep_route_plan.restype = _I32
+    L.ep_route_plan_noalloc.argtypes = [_P, _I64, _I32, _I32, _I32, _I64, _P, _P, _P, _P, _P]
+    L.ep_route_plan_noalloc.restype = _I32
     L.ep_nvfp4_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _I32, _U64, _P, _P]
     L.ep_nvfp4_pack.restype = _I32
     L.ep_nvfp4_unpack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _P]

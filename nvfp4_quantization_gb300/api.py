@@ -93,6 +93,19 @@ def ep_route_plan(topk_idx: torch.Tensor, E: int, A: int = DEFAULT_ALIGNMENT, R_
     return plan
 
 
+def ep_route_plan_noalloc(topk_idx: torch.Tensor, plan: RoutePlan, stream=None) -> RoutePlan:
+    """ep_route_plan into a caller-allocated ``plan``, with no workspace: the
+    C entry point uses a fixed scratch array inside the library and allocates
+    nothing (for hosts that own all device memory themselves).  Calls whose
+    work may overlap on one GPU share that scratch and race."""
+    _need_cuda(topk_idx, "topk_idx", torch.int32)
+    T, k = topk_idx.shape
+    st = _lib.lib().ep_route_plan_noalloc(_ptr(topk_idx), T, k, plan.E, plan.A, plan.R_cap, _ptr(plan.offsets),
+                                          _ptr(plan.counts), _ptr(plan.dest), _ptr(plan.status), _stream(stream))
+    check("ep_route_plan_noalloc", st)
+    return plan
+
+
 def ep_nvfp4_pack(tokens: torch.Tensor, plan: RoutePlan, rows: torch.Tensor | None = None,
                   rounding: int = EP_ROUND_RNE, seed: int = 0, stream=None) -> torch.Tensor:
     """BF16 tokens [T, H] -> packed NVFP4 rows [R_cap, row_bytes(H)] (uint8)."""

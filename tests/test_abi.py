@@ -98,3 +98,8 @@ def test_receive_and_unpack_validation():
     assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, ctypes.byref(g), 7, 0, 0, FAKE, None) == -5
     assert L.ep_nvfp4_unpack(FAKE, 128, 1000, FAKE, 4, FAKE, FAKE, None) == -2
     assert L.ep_nvfp4_unpack(None, 128, 1024, FAKE, 4, FAKE, FAKE, None) == -1
+
+
+def test_static_scratch_size_matches_header():
+    m = re.search(r"#define\s+EP_ROUTE_STATIC_SCRATCH_BYTES\s+(\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == _lib.EP_ROUTE_STATIC_SCRATCH_BYTES
