@@ -19,8 +19,9 @@
  * - Pointers named "device" are CUDA device memory owned by the caller; the
  *   library never allocates, frees or synchronises, and never keeps a pointer
  *   after the call returns.  Every call only enqueues work on `stream` (a
- *   cudaStream_t passed as void*; NULL = the legacy default stream), so every
- *   call can be captured in a CUDA graph.
+ *   cudaStream_t passed as void*; NULL = the legacy default stream), so these
+ *   calls can be captured in a CUDA graph (ep_route_plan_noalloc aside: this
+ *   header makes no statement about capturing it).
  * - Device guard: the call makes the device that owns the first input pointer
  *   current for its duration (and restores the previous device); every other
  *   pointer must live on that same device, else EP_ERR_DEVICE (TE PR #3753,
@@ -228,9 +229,8 @@ typedef struct {
  * and 16-row block: y = (1/4) H16 diag(sigma) d over the decoded values d;
  * s = E4M3_RNE_sat(max|y| * (S_enc/6)); code = E2M1(|y| * (S_enc/s)) with the
  * sign of y (FP32, single-rounded operations, in this order).
- * One kernel: each CTA first reduces the row trailers of the experts its tiles
- * belong to (4 bytes per row) while its first tile loads are in flight, then
- * transforms its tiles.
+ * Two kernels on `stream`: the per-expert metadata from the row trailers (4
+ * bytes per row), then the tile transform, which reads S_enc back.
  */
 ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
                                   int64_t H, const int32_t *expert_offsets,

@@ -117,15 +117,13 @@ __device__ __forceinline__ uint2 encode_block16(const uint32_t *w, float s, floa
         } else {
             q = make_float2(__fdiv_rn(x.x, -s), __fdiv_rn(x.y, -s));
         }
-        if (kSR) {
-            const uint32_t rw = rnd[i >> 1];
-            const int sh = (i & 1) * 16;
-            q.x = sr_e2m1_value(q.x, (rw >> sh) & 0xffu);
-            q.y = sr_e2m1_value(q.y, (rw >> (sh + 8)) & 0xffu);
-        }
         v[2 * i] = q.x;
         v[2 * i + 1] = q.y;
     }
+    if (kSR) // element i takes random byte i % 4 of rnd[i / 4]
+        return make_uint2(cvt_e2m1x8_sr(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], rnd[0], rnd[1]) ^ 0x88888888u,
+                          cvt_e2m1x8_sr(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15], rnd[2], rnd[3]) ^
+                              0x88888888u);
     return make_uint2(cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]) ^ 0x88888888u,
                       cvt_e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]) ^ 0x88888888u);
 }

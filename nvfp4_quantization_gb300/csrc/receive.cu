@@ -1,5 +1,5 @@
 // Direct receive: packed NVFP4 rows -> the expert GEMM's grouped rowwise and
-// columnwise-RHT NVFP4 operands, in one pass over the rows, in one kernel.
+// columnwise-RHT NVFP4 operands, in one pass over the rows' data.
 //
 // TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR description:
 // the receiver builds the NVFP4 GroupedTensor straight from the rows in one
@@ -10,18 +10,20 @@
 // columnwise amax is bounded by 4x the rowwise amax.
 //
 // Work unit: a tile of 128 rows x 256 hidden columns (a tile never straddles
-// two experts: expert slots are multiples of 128 rows).  Each persistent CTA
-// owns a contiguous range of tiles and walks it column-strip by column-strip
-// (consecutive tiles of a strip complete each other's columnwise output
-// sectors), so it meets only one or two experts.
+// two experts: expert slots are multiples of 128 rows).  Tiles are numbered
+// strip-major and each persistent CTA owns a contiguous range of them, so a
+// CTA walks down one 256-column strip: each hidden column's columnwise codes
+// and scales leave it as one contiguous run of rows.
+//
+// Two launches.  expert_amax_kernel reduces each expert's 4-byte token
+// amaxes from the row trailers (the rows' data is not read) into the expert's
+// metadata and encode scale S_enc.  The tile kernel, launched behind it with
+// programmatic dependent launch, reads the offsets and S_enc once per CTA.
 //
 // Producer warp: streams tiles into a 3-stage shared-memory ring with 2-D TMA
-// loads (codes 128 B x 128 rows, scales 16 B x 128, row trailers 16 B x 128).
-// While a tile's loads are in flight it finds the tile's expert and, the
-// first time the CTA meets that expert, reduces the expert's 4-byte token
-// amaxes from the row trailers (the rows' data is not read again) into the
-// encode scale S_enc; the tile's expert, offsets and S_enc go into the stage
-// before the stage's barrier is released.
+// loads (codes 128 B x 128 rows, scales 16 B x 128, row trailers 16 B x 128);
+// the tile's expert, offsets and S_enc go into the stage before the stage's
+// barrier is released.
 //
 // Consumer warps (8): the rowwise operand leaves straight from the ring (TMA
 // store of the codes; 16-byte stores of the scales and the token scale).  For
@@ -53,10 +55,9 @@ constexpr uint32_t kStageTx = kTileRows * (kCodeBytes + kScaleBytes + 16);
 constexpr int kWarpRows = kTileRows / 2;     // rows of a tile one consumer warp handles
 constexpr int kWTabStride = kWarpRows + 2;   // float2 entries; pad: a warp's 4 column blocks hit distinct banks
 constexpr int kMaxExperts = 1024;
-constexpr int kSlots = 8;                    // experts per CTA with precomputed S_enc / s tables
 
 struct StageMeta {
-    int e, off, n, slot; // slot < 0: the expert's tables are computed per tile
+    int e, off, n;
     float se, ce;        // S_enc and fl32(S_enc / 6)
 };
 
@@ -65,8 +66,7 @@ struct __align__(128) DrSmem {
     uint8_t scales[kStages][kTileRows][kScaleBytes];
     uint32_t trailer[kStages][kTileRows][4];
     float2 wtab[kConsumerWarps][4][kWTabStride]; // per warp: [column block][row] decode scale, twice
-    float wrtab[kConsumerWarps][128];           // per warp: S_enc / s when the expert has no slot
-    float rtab[kSlots][128];                    // [slot][E4M3 code] -> fl32(S_enc / s)
+    float wrtab[kConsumerWarps][128];           // per warp: [E4M3 code s] -> fl32(S_enc / s) of its expert
     StageMeta meta[kStages];
     float se_cache[kMaxExperts];                // S_enc of the experts this CTA meets
     int offs[kMaxExperts + 1];                  // expert_offsets, copied once
@@ -87,50 +87,37 @@ struct DrArgs {
     int H;
     int R_cap;
     int n_strips;
+    int n_row_tiles;   // R / 128, set on the device
     uint8_t *rw_scales;
     float *rw_row_scale;
     uint8_t *cw_codes;
     uint8_t *cw_scales;
-    float *amax_row;
-    float *amax_col;
-    float *scale_enc;
+    const float *scale_enc;
     uint64_t seed;
     uint32_t sign_mask;
     uint32_t *status;
     int do_rowwise;
+    int cw_v8;         // cw_codes is 32-byte aligned: 32-byte stores
 };
 
-// Tiles [lo, hi) of this CTA (a contiguous share of all tiles), visited
-// strip by strip: for each column strip, the CTA's row tiles in order.
+// Tiles [lo, hi) of this CTA, a contiguous share of all tiles numbered
+// strip-major (u = strip * n_row_tiles + row_tile): consecutive tiles of a CTA
+// are consecutive 128-row tiles of one 256-column strip, so each hidden
+// column's columnwise codes and scales leave the CTA as one growing
+// contiguous run.
 struct TileWalk {
-    int lo, hi, rt0, rt1, ns, st, rt;
-    __device__ __forceinline__ void init(int n_units, int n_strips)
+    int u, hi, nrt;
+    __device__ __forceinline__ void init(int n_units, int n_row_tiles)
     {
         const int64_t G = gridDim.x, b = blockIdx.x;
-        lo = (int)(b * n_units / G);
+        u = (int)(b * n_units / G) - 1;
         hi = (int)((b + 1) * n_units / G);
-        ns = n_strips;
-        rt0 = lo / ns;
-        rt1 = hi > lo ? (hi - 1) / ns : rt0 - 1;
-        st = 0;
-        rt = rt0 - 1;
+        nrt = n_row_tiles;
     }
     // Advance to the next tile; false when the CTA's share is exhausted.
-    __device__ __forceinline__ bool next()
-    {
-        if (hi <= lo)
-            return false;
-        for (;;) {
-            if (++rt > rt1) {
-                rt = rt0;
-                if (++st >= ns)
-                    return false;
-            }
-            const int u = rt * ns + st;
-            if (u >= lo && u < hi)
-                return true;
-        }
-    }
+    __device__ __forceinline__ bool next() { return ++u < hi; }
+    __device__ __forceinline__ int rt() const { return u % nrt; }
+    __device__ __forceinline__ int st() const { return u / nrt; }
 };
 
 // Last e with offs[e] <= row (offs in shared memory).
@@ -164,23 +151,22 @@ __device__ __forceinline__ int producer_preissue(DrSmem &sm, const CUtensorMap *
 {
     int n = 0;
     TileWalk tw;
-    tw.init(n_units, p.n_strips);
+    tw.init(n_units, p.n_row_tiles);
     while (n < kStages && tw.next()) {
-        issue_tile(sm, tmc, tms, tmt, n, tw.rt, tw.st);
+        issue_tile(sm, tmc, tms, tmt, n, tw.rt(), tw.st());
         ++n;
     }
     return n;
 }
 
 __device__ __forceinline__ int producer_loop(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
-                                             const CUtensorMap *tmt, const DrArgs &p, int n_units, int pre,
-                                             int e0)
+                                             const CUtensorMap *tmt, const DrArgs &p, int n_units, int pre)
 {
     int issued = pre;
     TileWalk tw;
-    tw.init(n_units, p.n_strips);
+    tw.init(n_units, p.n_row_tiles);
     for (int it = 0; tw.next(); ++it) {
-        const int rt = tw.rt, st = tw.st;
+        const int rt = tw.rt(), st = tw.st();
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
         if (it >= pre) {
@@ -198,81 +184,80 @@ __device__ __forceinline__ int producer_loop(DrSmem &sm, const CUtensorMap *tmc,
         const int off = sm.offs[e];
         const int n = sm.offs[e + 1] - off;
         const float se = sm.se_cache[e];
-        const int slot = e - e0 < kSlots ? e - e0 : -1;
-        sm.meta[s] = StageMeta{e, off, n, slot, se, __fdiv_rn(se, 6.0f)};
+        sm.meta[s] = StageMeta{e, off, n, se, __fdiv_rn(se, 6.0f)};
         mbar_arrive(&sm.full[s]); // releases the metadata with the stage
     }
     return issued;
 }
 
-// Prologue (whole CTA): S_enc of every expert the CTA's tiles belong to, from
-// the 4-byte token amaxes in the row trailers (eight loads in flight per
-// thread, issued before the first tile loads so they do not queue behind
-// them), plus the table S_enc / s over all E4M3 codes s for the first kSlots
-// experts; the CTA holding an expert's first tile of strip 0 also writes the
-// expert's metadata.  Returns the CTA's first expert.
-__device__ __forceinline__ int expert_prologue(DrSmem &sm, const DrArgs &p, int n_units, uint32_t *red,
-                                               const CUtensorMap *tmc, const CUtensorMap *tms,
-                                               const CUtensorMap *tmt, int *pre)
+// Per-expert metadata (one CTA per expert, grid-stride): the rowwise amax is
+// the largest 4-byte token amax in the expert's row trailers (the rows' data
+// is not read), the columnwise amax its 4x bound, S_enc = 2688 / amax_col.
+// The tile kernel that follows reads S_enc back.
+constexpr int kAmaxThreads = 512;
+
+__global__ void __launch_bounds__(kAmaxThreads)
+expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *__restrict__ offsets, int E,
+                   int R_cap, float *__restrict__ amax_row, float *__restrict__ amax_col,
+                   float *__restrict__ scale_enc)
 {
-    const int64_t G = gridDim.x, b = blockIdx.x;
-    const int lo = (int)(b * n_units / G), hi = (int)((b + 1) * n_units / G);
-    const bool producer = threadIdx.x == kConsumers;
-    if (lo >= hi)
-        return 0;
-    const int e0 = expert_of_row(sm.offs, p.E, (lo / p.n_strips) * kTileRows);
-    const int e1 = expert_of_row(sm.offs, p.E, ((hi - 1) / p.n_strips) * kTileRows);
-    const int tid = threadIdx.x, nt = blockDim.x;
-    for (int e = e0; e <= e1; ++e) {
-        const int off = sm.offs[e];
-        const int end = min(sm.offs[e + 1], p.R_cap);
+    __shared__ uint32_t red[kAmaxThreads / 32];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tid = threadIdx.x;
+    const uint8_t *amax_at = rows + S - 12;   // A_t inside each row's trailer
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int off = __ldg(offsets + e);
+        const int end = min(__ldg(offsets + e + 1), R_cap);
         uint32_t m = 0; // non-negative floats compare as their bit patterns
-        for (int r = off + tid; r < end; r += 8 * nt) {
+        for (int r = off + tid; r < end; r += 8 * kAmaxThreads) {
             uint32_t v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int rr = r + j * nt;
-                v[j] = rr < end ? __ldg(reinterpret_cast<const uint32_t *>(p.rows + (int64_t)rr * p.S + p.S - 12)) : 0u;
+                const int rr = r + j * kAmaxThreads;
+                v[j] = rr < end ? __ldg(reinterpret_cast<const uint32_t *>(amax_at + (int64_t)rr * S)) : 0u;
             }
-            if (producer && e == e0 && r == off + tid)
-                *pre = producer_preissue(sm, tmc, tms, tmt, p, n_units);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 m = max(m, v[j]);
         }
-        if (producer && e == e0 && off + tid >= end)
-            *pre = producer_preissue(sm, tmc, tms, tmt, p, n_units);
         m = __reduce_max_sync(0xffffffffu, m);
         if ((tid & 31) == 0)
             red[tid >> 5] = m;
         __syncthreads();
-        m = 0u;
-        for (int w = 0; w < (nt + 31) / 32; ++w)
-            m = max(m, red[w]);
-        const float a = u2f(m), ac = 4.0f * a;
-        const float se = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
         if (tid == 0) {
-            sm.se_cache[e] = se;
-            const int u_owner = (off / kTileRows) * p.n_strips; // strip 0 of the expert's first tile
-            if (end > off && u_owner >= lo && u_owner < hi) {
-                p.amax_row[e] = a;
-                p.amax_col[e] = ac;
-                p.scale_enc[e] = se;
-            }
-        }
-        if (e - e0 < kSlots && tid < 128) {
-            const float sv = e4m3_to_f32((uint32_t)tid);
-            sm.rtab[e - e0][tid] = (sv == 0.0f) ? 0.0f : __fdiv_rn(se, sv);
+            uint32_t x = 0u;
+            for (int w = 0; w < kAmaxThreads / 32; ++w)
+                x = max(x, red[w]);
+            const float a = u2f(x), ac = 4.0f * a;
+            amax_row[e] = a;
+            amax_col[e] = ac;
+            scale_enc[e] = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
         }
         __syncthreads();
     }
-    return e0;
+}
+
+// Tile-kernel set-up after the wait on the amax kernel (expert offsets and
+// S_enc of every expert are in shared memory): the first tile loads.
+__device__ __forceinline__ int tile_prologue(DrSmem &sm, const DrArgs &p, int n_units, const CUtensorMap *tmc,
+                                             const CUtensorMap *tms, const CUtensorMap *tmt)
+{
+    return threadIdx.x == kConsumers ? producer_preissue(sm, tmc, tms, tmt, p, n_units) : 0;
 }
 
 __device__ __forceinline__ void st16g(void *p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
+                 : "memory");
+}
+
+// 32-byte store (one full sector); p must be 32-byte aligned.
+__device__ __forceinline__ void st32g(void *p, uint4 a, uint4 b)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y),
+                 "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
                  : "memory");
 }
 
@@ -322,16 +307,17 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
     for (int i = 0; i < 16; ++i)
         u[i] = mul2(u[i], r2);
     if (kSR) {
+        // row i of the block takes random byte i of its column's 16 bytes
         const uint64_t pos = (uint64_t)m.off * (uint64_t)p.H + (uint64_t)h0 * (uint64_t)m.n + (uint64_t)(rl + r0);
         const Philox4 ra = sr_bytes16(p.seed, 1u, pos);
         const Philox4 rb = sr_bytes16(p.seed, 1u, pos + (uint64_t)m.n);
-        const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
-        const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            u[i].x = sr_e2m1_value(u[i].x, (wa[i >> 2] >> (8 * (i & 3))) & 0xffu);
-            u[i].y = sr_e2m1_value(u[i].y, (wb[i >> 2] >> (8 * (i & 3))) & 0xffu);
-        }
+        cw0 = make_uint2(cvt_e2m1x8_sr(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x, ra.x, ra.y),
+                         cvt_e2m1x8_sr(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x, ra.z,
+                                       ra.w));
+        cw1 = make_uint2(cvt_e2m1x8_sr(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y, rb.x, rb.y),
+                         cvt_e2m1x8_sr(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y, rb.z,
+                                       rb.w));
+        return;
     }
     cw0 = make_uint2(cvt_e2m1x8(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x),
                      cvt_e2m1x8(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x));
@@ -350,10 +336,11 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
     const int H = p.H;
     float2(*tab)[kWTabStride] = sm.wtab[warp];
     int done = 0;
+    int cur_e = -1;   // expert whose S_enc / s table this warp holds
     TileWalk tw;
-    tw.init(n_units, p.n_strips);
+    tw.init(n_units, p.n_row_tiles);
     for (int it = 0; tw.next(); ++it) {
-        const int rt = tw.rt, st = tw.st;
+        const int rt = tw.rt(), st = tw.st();
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
         if (!mbar_wait_bounded(&sm.full[s], ph) || sm.abort_flag) {
@@ -403,8 +390,9 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
             tab[2][rloc] = make_float2(v2, v2);
             tab[3][rloc] = make_float2(v3, v3);
         }
-        const float *rtab = m.slot >= 0 ? sm.rtab[m.slot] : sm.wrtab[warp];
-        if (m.slot < 0) {
+        const float *rtab = sm.wrtab[warp];
+        if (m.e != cur_e) {
+            cur_e = m.e;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int code = lane + 32 * q;
@@ -420,17 +408,28 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
             uint8_t *d0 = p.cw_codes + (int64_t)m.off * (H / 2) + (int64_t)h0 * (m.n / 2) + (rl + 64 * hh) / 2;
             uint8_t *d1 = d0 + (m.n / 2);
             uint32_t sc0 = 0u, sc1 = 0u;
-#pragma unroll 1
+            uint4 q0[2], q1[2];   // 32 bytes (64 rows) of codes of columns h0 and h0 + 1
+#pragma unroll
             for (int bp = 0; bp < 2; ++bp) {
                 uint2 a0, a1, b0, b1;
                 uint32_t s2a, s2b;
                 const int r0 = 64 * hh + 32 * bp;
                 rht_block<kSR>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, p, m, h0, rl, a0, a1, s2a);
                 rht_block<kSR>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, p, m, h0, rl, b0, b1, s2b);
-                st16g(d0 + 16 * bp, make_uint4(a0.x, a0.y, b0.x, b0.y));
-                st16g(d1 + 16 * bp, make_uint4(a1.x, a1.y, b1.x, b1.y));
+                q0[bp] = make_uint4(a0.x, a0.y, b0.x, b0.y);
+                q1[bp] = make_uint4(a1.x, a1.y, b1.x, b1.y);
                 sc0 |= ((s2a & 0xffu) | ((s2b & 0xffu) << 8)) << (16 * bp);
                 sc1 |= (((s2a >> 8) & 0xffu) | (((s2b >> 8) & 0xffu) << 8)) << (16 * bp);
+            }
+            // one full 32-byte sector per column when the buffer allows it
+            if (p.cw_v8) {
+                st32g(d0, q0[0], q0[1]);
+                st32g(d1, q1[0], q1[1]);
+            } else {
+                st16g(d0, q0[0]);
+                st16g(d0 + 16, q0[1]);
+                st16g(d1, q1[0]);
+                st16g(d1 + 16, q1[1]);
             }
             uint8_t *cs = p.cw_scales + (int64_t)m.off * (H / 16) + (int64_t)h0 * (m.n / 16) + (rl + 64 * hh) / 16;
             *reinterpret_cast<uint32_t *>(cs) = sc0;
@@ -451,7 +450,7 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
 }
 
 template <bool kSR>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __maxnreg__(104)
 direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
                       const __grid_constant__ CUtensorMap tm_scales,
                       const __grid_constant__ CUtensorMap tm_trailer,
@@ -479,8 +478,11 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     pdl_launch_dependents();
     pdl_wait();
 
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x)
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
         sm.offs[i] = __ldg(p.offsets + i);
+        if (i < p.E)
+            sm.se_cache[i] = p.scale_enc[i];
+    }
     __syncthreads();
     int R = sm.offs[p.E];
     if (R > p.R_cap) {
@@ -488,26 +490,15 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
             raise_status(p.status, kDevErrCapacity);
         R = p.R_cap;
     }
-    const int n_units = (R / kTileRows) * p.n_strips;
+    p.n_row_tiles = R / kTileRows;
+    const int n_units = p.n_row_tiles * p.n_strips;
 
-    __shared__ uint32_t red[kThreads / 32];
-    int pre = 0;
-    const int e0 = expert_prologue(sm, p, n_units, red, &tm_codes, &tm_scales, &tm_trailer, &pre);
+    const int pre = tile_prologue(sm, p, n_units, &tm_codes, &tm_scales, &tm_trailer);
 
     int issued = 0;
     if (warp == kConsumerWarps) {
         if (lane == 0)
-            issued = producer_loop(sm, &tm_codes, &tm_scales, &tm_trailer, p, n_units, pre, e0);
-        // metadata of the experts that own no rows
-        if (blockIdx.x == 0) {
-            for (int e = lane; e < p.E; e += 32) {
-                if (__ldg(p.offsets + e + 1) == __ldg(p.offsets + e)) {
-                    p.amax_row[e] = 0.0f;
-                    p.amax_col[e] = 0.0f;
-                    p.scale_enc[e] = 1.0f;
-                }
-            }
-        }
+            issued = producer_loop(sm, &tm_codes, &tm_scales, &tm_trailer, p, n_units, pre);
     } else {
         const int done = consumer_loop<kSR>(sm, &tm_rw, p, n_units);
         if (threadIdx.x == 0)
@@ -554,33 +545,16 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Empty-expert metadata when no tile kernel runs (R_cap < one tile).
-__global__ void small_meta_kernel(const uint8_t *rows, int64_t S, const int32_t *offsets, int E, int R_cap,
-                                  float *amax_row, float *amax_col, float *scale_enc)
-{
-    pdl_launch_dependents();
-    pdl_wait();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        uint32_t m = 0;
-        const int hi = min(offsets[e + 1], R_cap);
-        for (int r = offsets[e]; r < hi; ++r)
-            m = max(m, *reinterpret_cast<const uint32_t *>(rows + (int64_t)r * S + S - 12));
-        const float a = u2f(m), ac = 4.0f * a;
-        amax_row[e] = a;
-        amax_col[e] = ac;
-        scale_enc[e] = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
-    }
-}
-
 cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
                                   const int32_t *offsets, int E, const GroupedOut &out,
                                   int rounding, uint64_t seed, uint32_t sign_mask,
                                   uint32_t *status)
 {
     const int64_t S = row_bytes(H);
-    if (R_cap < kTileRows)
-        return launch_pdl(small_meta_kernel, dim3(1), dim3(256), 0, c.stream, rows, S, offsets, E, R_cap,
-                          out.amax_row, out.amax_col, out.scale_enc);
+    cudaError_t err = launch_pdl(expert_amax_kernel, dim3((unsigned)E), dim3(kAmaxThreads), 0, c.stream, rows, S,
+                                 offsets, E, R_cap, out.amax_row, out.amax_col, out.scale_enc);
+    if (err != cudaSuccess || R_cap < kTileRows)   // fewer than 128 rows of capacity: no tile can exist
+        return err;
 
     CUtensorMap tm_codes, tm_scales, tm_trailer, tm_rw;
     memset(&tm_rw, 0, sizeof(tm_rw));
@@ -605,17 +579,16 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     a.rw_row_scale = out.rw_row_scale;
     a.cw_codes = out.cw_codes;
     a.cw_scales = out.cw_scales;
-    a.amax_row = out.amax_row;
-    a.amax_col = out.amax_col;
     a.scale_enc = out.scale_enc;
     a.seed = seed;
     a.sign_mask = sign_mask;
     a.status = status;
     a.do_rowwise = do_rw;
+    a.cw_v8 = (reinterpret_cast<uintptr_t>(out.cw_codes) & 31u) == 0;
 
     const size_t smem = sizeof(DrSmem) + 1024;
     static int done_rn[2] = {0, 0}, done_sr[2] = {0, 0};
-    cudaError_t err = rounding == 1 ? ensure_smem_limit(direct_receive_kernel<true>, c.device, (int)smem, done_sr)
+    err = rounding == 1 ? ensure_smem_limit(direct_receive_kernel<true>, c.device, (int)smem, done_sr)
                                     : ensure_smem_limit(direct_receive_kernel<false>, c.device, (int)smem, done_rn);
     if (err != cudaSuccess)
         return err;

@@ -75,19 +75,28 @@ __device__ int block_exclusive_scan(int *a, int n, int *wtmp)
 // Grid-wide barrier over a cooperative launch.  Self-resetting: the last CTA
 // to arrive zeroes the count and bumps the generation the others wait on, so
 // the two workspace words are back to a usable state after every call (they
-// must be zero before the first call).  Bounded: gives up after ~1 s.
-__device__ bool grid_barrier(uint32_t *count, uint32_t *gen, uint32_t n, int *flag)
+// must be zero before the first call).  `g` is the generation thread 0 read
+// at kernel start: it cannot change before this CTA arrives.  Arrival is one
+// acquire-release atomic (it publishes this CTA's writes, and the last CTA
+// acquires everyone's before its release of the generation), so no separate
+// fences are needed.  Bounded: gives up after ~1 s.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ bool grid_barrier(uint32_t *count, uint32_t *gen, uint32_t g, uint32_t n, int *flag)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        const uint32_t g = ld_acquire_gpu(gen);
-        __threadfence();
-        const uint32_t arrived = atomicAdd(count, 1u) + 1u;
-        if (arrived == n) {
-            atomicExch(count, 0u);
-            __threadfence();
-            atomicAdd(gen, 1u);
+        uint32_t old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(count) : "memory");
+        if (old + 1u == n) {
+            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(count), "r"(0u) : "memory");
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gen) : "memory");
         } else {
             ok = 0;
             for (uint32_t i = 0; i < (1u << 23); ++i) {
@@ -99,7 +108,6 @@ __device__ bool grid_barrier(uint32_t *count, uint32_t *gen, uint32_t n, int *fl
                     __nanosleep(128);
             }
         }
-        __threadfence();
         *flag = ok;
     }
     __syncthreads();
@@ -130,6 +138,7 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x, nctas = gridDim.x;
     int32_t *hist = reinterpret_cast<int32_t *>(ws + kWsHeader);   // [nctas][E]
+    const uint32_t g0 = tid == 0 ? ld_relaxed_gpu(ws + 1) : 0u;  // barrier generation before arrival
     const int64_t t = (int64_t)cta * kChunk + tid;
 
     int raw[kRegSlots], ev[kRegSlots], rk[kRegSlots];
@@ -188,7 +197,7 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
         rk[j] = e >= 0 ? (int)(pre[e * kWords + warp] + __popc(mask[e * kWords + warp] & ((1u << lane) - 1u))) : 0;
     }
 
-    if (!grid_barrier(ws, ws + 1, (uint32_t)nctas, &flag)) {
+    if (!grid_barrier(ws, ws + 1, g0, (uint32_t)nctas, &flag)) {
         if (tid == 0)
             raise_status(status, kDevErrTimeout);
         return;
@@ -196,6 +205,7 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
 
     for (int e = tid; e < E; e += kChunk) {
         int p = 0, all = 0;
+#pragma unroll 8
         for (int c = 0; c < nctas; ++c) {
             const int h = __ldcg(hist + (int64_t)c * E + e);
             p += (c < cta) ? h : 0;
@@ -244,6 +254,7 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x, nctas = gridDim.x;
     int32_t *hist = reinterpret_cast<int32_t *>(ws + kWsHeader);   // [nctas][E]
+    const uint32_t g0 = tid == 0 ? ld_relaxed_gpu(ws + 1) : 0u;  // barrier generation before arrival
     for (int e = tid; e < E; e += kChunk)
         run[e] = 0;
 
@@ -315,7 +326,7 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
     for (int e = tid; e < E; e += kChunk)
         hist[(int64_t)cta * E + e] = run[e];
 
-    if (!grid_barrier(ws, ws + 1, (uint32_t)nctas, &flag)) {
+    if (!grid_barrier(ws, ws + 1, g0, (uint32_t)nctas, &flag)) {
         if (tid == 0)
             raise_status(status, kDevErrTimeout);
         return;
@@ -324,6 +335,7 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
     // ---- phase 2: offsets, and global rows of this CTA's slots
     for (int e = tid; e < E; e += kChunk) {
         int p = 0, tot = 0;
+#pragma unroll 8
         for (int c = 0; c < nctas; ++c) {
             const int h = __ldcg(hist + (int64_t)c * E + e);
             p += (c < cta) ? h : 0;
