@@ -280,6 +280,14 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
     return out != 0;
 }
 
+// max(m, |a|, |b|) in one three-input maximum (finite inputs).
+__device__ __forceinline__ float max3_abs(float m, float a, float b)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+    return d;
+}
+
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
 // as 1, 2, 3", SC'11): ten rounds, each two 32x32->64-bit products of words 0
@@ -290,21 +298,40 @@ struct Philox4 {
     uint32_t x, y, z, w;
 };
 
+// The ten round keys of one seed, (k0 + r W0, k1 + r W1) for r = 0..9 with
+// (k0, k1) the low and high words of the seed and (W0, W1) the Weyl
+// constants, computed once on the host and passed as a kernel parameter so
+// the rounds read them straight from the constant bank.
+struct PhiloxKey {
+    uint32_t k[10][2];
+};
+
+__host__ __device__ inline PhiloxKey philox_key(uint64_t seed)
+{
+    PhiloxKey K;
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        K.k[r][0] = k0;
+        K.k[r][1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return K;
+}
+
 __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                                 uint32_t k0, uint32_t k1)
+                                                 const PhiloxKey &K)
 {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
-        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
-        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
-        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ K.k[r][0];
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ K.k[r][1];
         c1 = (uint32_t)p1;
         c3 = (uint32_t)p0;
         c0 = n0;
         c2 = n2;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
     }
     return Philox4{c0, c1, c2, c3};
 }
@@ -312,11 +339,10 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
 // The 16 random bytes of the aligned group of 16 elements starting at element
 // index idx0 (idx0 % 16 == 0) of stream `stream`: byte i of the result (word
 // i/4, byte i%4, little-endian) belongs to element idx0 + i.
-__device__ __forceinline__ Philox4 sr_bytes16(uint64_t seed, uint32_t stream, uint64_t idx0)
+__device__ __forceinline__ Philox4 sr_bytes16(const PhiloxKey &K, uint32_t stream, uint64_t idx0)
 {
-    uint64_t n = idx0 >> 4;
-    return philox4x32_10((uint32_t)n, (uint32_t)(n >> 32), stream, 0u, (uint32_t)seed,
-                         (uint32_t)(seed >> 32));
+    const uint64_t n = idx0 >> 4;
+    return philox4x32_10((uint32_t)n, (uint32_t)(n >> 32), stream, 0u, K);
 }
 
 // Eight FP32 values -> one word of eight E2M1 codes by stochastic rounding,
@@ -333,26 +359,33 @@ __device__ __forceinline__ Philox4 sr_bytes16(uint64_t seed, uint32_t stream, ui
 // same two numbers bit-reversed), rounding up iff |fraction| + R >= 1.  With
 // rbits[15:0] = 0 this is exactly the 8-bit rule above for operands 1 and 3,
 // so each conversion here carries two values, in operands 1 and 3.
-__device__ __forceinline__ uint32_t cvt_e2m1x2_sr(float even, float odd, uint32_t rbits)
-{
-    uint16_t o;
-    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
-        : "=h"(o)
-        : "f"(0.0f), "f"(odd), "f"(0.0f), "f"(even), "r"(rbits));
-    return o;   // odd element's code in bits 8..11, even element's in bits 0..3
-}
-
+//
+// Pairing: conversion j takes elements (j', j' + 2) of a group of four in
+// operands 3 and 1 (random bytes j' and j' + 2 moved to rbits[23:16] and
+// rbits[31:24] by one byte permute with zero), so the four 16-bit results
+// packed as (even elements | odd elements << 4) are the final word.
 __device__ __forceinline__ uint32_t cvt_e2m1x8_sr(float a0, float a1, float a2, float a3, float a4, float a5,
                                                   float a6, float a7, uint32_t r_lo, uint32_t r_hi)
 {
-    // random bytes 2j, 2j+1 into rbits[23:16], rbits[31:24]; rbits[15:0] = 0
-    const uint32_t t0 = __byte_perm(cvt_e2m1x2_sr(a0, a1, __byte_perm(r_lo, 0u, 0x1044)),
-                                    cvt_e2m1x2_sr(a2, a3, __byte_perm(r_lo, 0u, 0x3244)), 0x5410);
-    const uint32_t t1 = __byte_perm(cvt_e2m1x2_sr(a4, a5, __byte_perm(r_hi, 0u, 0x1044)),
-                                    cvt_e2m1x2_sr(a6, a7, __byte_perm(r_hi, 0u, 0x3244)), 0x5410);
-    // t = c1 << 8 | c0 | c3 << 24 | c2 << 16: fold each odd code next to its
-    // even neighbour, then keep bytes 0 and 2 of each half
-    return __byte_perm(t0 | (t0 >> 4), t1 | (t1 >> 4), 0x6420);
+    uint32_t out;
+    asm("{\n\t.reg .b16 h0, h1, h2, h3;\n\t"
+        ".reg .b32 q0, q1, q2, q3, e, o;\n\t"
+        "prmt.b32 q0, %9, 0, 0x2044;\n\t"
+        "prmt.b32 q1, %9, 0, 0x3144;\n\t"
+        "prmt.b32 q2, %10, 0, 0x2044;\n\t"
+        "prmt.b32 q3, %10, 0, 0x3144;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h0, {%11, %3, %11, %1}, q0;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h1, {%11, %4, %11, %2}, q1;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h2, {%11, %7, %11, %5}, q2;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h3, {%11, %8, %11, %6}, q3;\n\t"
+        "mov.b32 e, {h0, h2};\n\t"
+        "mov.b32 o, {h1, h3};\n\t"
+        "shl.b32 o, o, 4;\n\t"
+        "or.b32 %0, e, o;\n\t}"
+        : "=r"(out)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7), "r"(r_lo), "r"(r_hi),
+          "f"(0.0f));
+    return out;
 }
 
 // Stochastic rounding of an FP32 value onto the E2M1 grid with an 8-bit random

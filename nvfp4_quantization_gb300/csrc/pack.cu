@@ -246,7 +246,7 @@ template <int CPT, bool kSR>
 __global__ void __launch_bounds__(kMaxThreads)
 nvfp4_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32_t *__restrict__ dest,
                   int k, const int32_t *__restrict__ offsets, const int32_t *__restrict__ counts, int E,
-                  uint8_t *__restrict__ rows, int64_t S, int R_cap, uint64_t seed,
+                  uint8_t *__restrict__ rows, int64_t S, int R_cap, const __grid_constant__ PhiloxKey key,
                   uint32_t *__restrict__ status, int n_tok_ctas, int pad_ctas,
                   const __grid_constant__ RcpTable rcp)
 {
@@ -311,8 +311,8 @@ nvfp4_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
             uint2 c0, c1;
             if (kSR) {
                 const uint64_t idx0 = (uint64_t)t * (uint64_t)H + (uint64_t)q * 32u;
-                const Philox4 r0 = sr_bytes16(seed, 0u, idx0);
-                const Philox4 r1 = sr_bytes16(seed, 0u, idx0 + 16u);
+                const Philox4 r0 = sr_bytes16(key, 0u, idx0);
+                const Philox4 r1 = sr_bytes16(key, 0u, idx0 + 16u);
                 const uint32_t rr0[4] = {r0.x, r0.y, r0.z, r0.w};
                 const uint32_t rr1[4] = {r1.x, r1.y, r1.z, r1.w};
                 c0 = encode_block16<true>(&w[c][0], s0, yn0, fast, rr0);
@@ -362,7 +362,7 @@ nvfp4_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
 // Encode NB blocks held by one lane (block b = lane + 32 b of the token).
 template <int NB, bool kFast, bool kSR>
 __device__ __forceinline__ void encode_lane_blocks(const uint32_t (&w)[NB][8], const uint32_t (&bm)[NB], float St,
-                                                   float inv_st, const float *srcp, uint64_t seed, uint64_t t,
+                                                   float inv_st, const float *srcp, const PhiloxKey &key, uint64_t t,
                                                    int H, int lane, uint2 (&code)[NB], uint32_t (&sbyte)[NB])
 {
 #pragma unroll
@@ -388,7 +388,7 @@ __device__ __forceinline__ void encode_lane_blocks(const uint32_t (&w)[NB][8], c
                 sbyte[bb] = sc;
                 if (kSR) {
                     const uint64_t idx0 = t * (uint64_t)H + (uint64_t)(lane + 32 * bb) * 16u;
-                    const Philox4 r = sr_bytes16(seed, 0u, idx0);
+                    const Philox4 r = sr_bytes16(key, 0u, idx0);
                     const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
                     code[bb] = encode_block16<true>(w[bb], s, yn, kFast, rr);
                 } else {
@@ -413,7 +413,7 @@ template <int NB, bool kSR>
 __global__ void __launch_bounds__(32 * kPackWarps)
 nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32_t *__restrict__ dest,
                        int k, const int32_t *__restrict__ offsets, const int32_t *__restrict__ counts, int E,
-                       uint8_t *__restrict__ rows, int64_t S, int R_cap, uint64_t seed,
+                       uint8_t *__restrict__ rows, int64_t S, int R_cap, const __grid_constant__ PhiloxKey key,
                        uint32_t *__restrict__ status, int n_tok_ctas, int pad_ctas,
                        const __grid_constant__ RcpTable rcp)
 {
@@ -507,9 +507,9 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
         uint2 code[NB];
         uint32_t sbyte[NB];
         if (kt >= -100 && kt <= 100)
-            encode_lane_blocks<NB, true, kSR>(w, bm, St, exp2i(-kt), srcp, seed, (uint64_t)t, H, lane, code, sbyte);
+            encode_lane_blocks<NB, true, kSR>(w, bm, St, exp2i(-kt), srcp, key, (uint64_t)t, H, lane, code, sbyte);
         else
-            encode_lane_blocks<NB, false, kSR>(w, bm, St, 0.0f, srcp, seed, (uint64_t)t, H, lane, code, sbyte);
+            encode_lane_blocks<NB, false, kSR>(w, bm, St, 0.0f, srcp, key, (uint64_t)t, H, lane, code, sbyte);
         for (int j = 0; j < k; ++j) {
             const int d = __shfl_sync(0xffffffffu, dl, j);
             if (d < 0)
@@ -642,9 +642,9 @@ static cudaError_t launch_nvfp4_cpt(const LaunchCtx &c, const uint16_t *tokens, 
         tc = 1;
     if (rounding == 1)
         return launch_pdl(nvfp4_pack_kernel<CPT, true>, dim3(tc + pc), dim3(th), 0, c.stream, tokens, T, H, dest,
-                          k, offsets, counts, E, rows, S, R_cap, seed, status, tc, pc, rcp);
+                          k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
     return launch_pdl(nvfp4_pack_kernel<CPT, false>, dim3(tc + pc), dim3(th), 0, c.stream, tokens, T, H, dest, k,
-                      offsets, counts, E, rows, S, R_cap, seed, status, tc, pc, rcp);
+                      offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
 }
 
 template <int NB>
@@ -679,9 +679,9 @@ static cudaError_t launch_nvfp4_warp(const LaunchCtx &c, const uint16_t *tokens,
         tc = 1;
     if (rounding == 1)
         return launch_pdl(nvfp4_pack_warp_kernel<NB, true>, dim3(tc + pc), dim3(th), smem, c.stream, tokens, T, H,
-                          dest, k, offsets, counts, E, rows, S, R_cap, seed, status, tc, pc, rcp);
+                          dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
     return launch_pdl(nvfp4_pack_warp_kernel<NB, false>, dim3(tc + pc), dim3(th), smem, c.stream, tokens, T, H,
-                      dest, k, offsets, counts, E, rows, S, R_cap, seed, status, tc, pc, rcp);
+                      dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
 }
 
 cudaError_t launch_nvfp4_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,

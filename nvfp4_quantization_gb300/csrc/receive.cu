@@ -10,10 +10,9 @@
 // columnwise amax is bounded by 4x the rowwise amax.
 //
 // Work unit: a tile of 128 rows x 256 hidden columns (a tile never straddles
-// two experts: expert slots are multiples of 128 rows).  Tiles are numbered
-// strip-major and each persistent CTA owns a contiguous range of them, so a
-// CTA walks down one 256-column strip: each hidden column's columnwise codes
-// and scales leave it as one contiguous run of rows.
+// two experts: expert slots are multiples of 128 rows).  Persistent CTAs take
+// the tiles in row-major order, round robin, so the whole grid sweeps the
+// rows once, front to back.
 //
 // Two launches.  expert_amax_kernel reduces each expert's 4-byte token
 // amaxes from the row trailers (the rows' data is not read) into the expert's
@@ -26,14 +25,16 @@
 // barrier is released.
 //
 // Consumer warps (8): the rowwise operand leaves straight from the ring (TMA
-// store of the codes; 16-byte stores of the scales and the token scale).  For
-// the columnwise operand each thread owns two adjacent hidden columns (one
-// code byte per row) and 64 of the 128 rows: it decodes 16 rows at a time
-// exactly into FP32 pairs with a per-tile table of (E4M3 block scale x token
-// scale x sigma / 4), runs the 16-point Walsh-Hadamard butterflies on packed
-// FP32 pairs, derives the E4M3 block scale from S_enc, re-encodes to E2M1
-// (RNE or Philox-driven stochastic rounding) and writes 16-byte chunks of the
-// [H][n_e] columnwise layout.
+// stores of the codes and, when H % 256 == 0, of the scales; the token scale
+// by threads).  For the columnwise operand each thread owns two adjacent
+// hidden columns (one code byte per row) and 64 of the 128 rows: it decodes
+// 16 rows at a time exactly into FP32 pairs with a per-tile table of (E4M3
+// block scale x token scale x sigma / 4), runs the 16-point Walsh-Hadamard
+// butterflies on packed FP32 pairs, derives the E4M3 block scale from S_enc,
+// re-encodes to E2M1 (RNE or Philox-driven stochastic rounding) and writes
+// each column's 32 code bytes as one sector of the [H][n_e] columnwise
+// layout; the warp holding rows 64..127 hands its scale bytes to the warp
+// holding rows 0..63 so each column's 8 scale bytes leave in one store.
 #include <cudaTypedefs.h>
 #include <float.h>
 #include <string.h>
@@ -67,11 +68,13 @@ struct __align__(128) DrSmem {
     uint32_t trailer[kStages][kTileRows][4];
     float2 wtab[kConsumerWarps][4][kWTabStride]; // per warp: [column block][row] decode scale, twice
     float wrtab[kConsumerWarps][128];           // per warp: [E4M3 code s] -> fl32(S_enc / s) of its expert
+    uint32_t csc[kStages][kConsumerWarps / 2][32][2]; // [stage][column quarter][lane]: scales of rows 64..127
     StageMeta meta[kStages];
     float se_cache[kMaxExperts];                // S_enc of the experts this CTA meets
     int offs[kMaxExperts + 1];                  // expert_offsets, copied once
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t csc_full[kStages][kConsumerWarps / 2];   // csc[stage][quarter] written
     int abort_flag;
     int consumed;
 };
@@ -87,37 +90,37 @@ struct DrArgs {
     int H;
     int R_cap;
     int n_strips;
-    int n_row_tiles;   // R / 128, set on the device
     uint8_t *rw_scales;
     float *rw_row_scale;
     uint8_t *cw_codes;
     uint8_t *cw_scales;
     const float *scale_enc;
-    uint64_t seed;
+    PhiloxKey key;     // round keys of the SR seed
     uint32_t sign_mask;
     uint32_t *status;
     int do_rowwise;
     int cw_v8;         // cw_codes is 32-byte aligned: 32-byte stores
+    int rws_tma;       // rowwise scales leave by TMA store (H % 256 == 0)
 };
 
-// Tiles [lo, hi) of this CTA, a contiguous share of all tiles numbered
-// strip-major (u = strip * n_row_tiles + row_tile): consecutive tiles of a CTA
-// are consecutive 128-row tiles of one 256-column strip, so each hidden
-// column's columnwise codes and scales leave the CTA as one growing
-// contiguous run.
+// Tiles of this CTA: u = blockIdx.x + k * gridDim.x, k = 0, 1, ... over the
+// tiles numbered row-major (u = row_tile * n_strips + strip).  At any moment
+// the grid works on one contiguous band of row tiles, all strips of each:
+// complete rowwise rows and, because expert slots are contiguous row ranges,
+// whole columnwise column runs are written within a short window, so the
+// output reaches DRAM in whole pages instead of scattered lines.
 struct TileWalk {
-    int u, hi, nrt;
-    __device__ __forceinline__ void init(int n_units, int n_row_tiles)
+    int u, n, ns;
+    __device__ __forceinline__ void init(int n_units, int n_strips)
     {
-        const int64_t G = gridDim.x, b = blockIdx.x;
-        u = (int)(b * n_units / G) - 1;
-        hi = (int)((b + 1) * n_units / G);
-        nrt = n_row_tiles;
+        u = (int)blockIdx.x - (int)gridDim.x;
+        n = n_units;
+        ns = n_strips;
     }
     // Advance to the next tile; false when the CTA's share is exhausted.
-    __device__ __forceinline__ bool next() { return ++u < hi; }
-    __device__ __forceinline__ int rt() const { return u % nrt; }
-    __device__ __forceinline__ int st() const { return u / nrt; }
+    __device__ __forceinline__ bool next() { return (u += (int)gridDim.x) < n; }
+    __device__ __forceinline__ int rt() const { return u / ns; }
+    __device__ __forceinline__ int st() const { return u % ns; }
 };
 
 // Last e with offs[e] <= row (offs in shared memory).
@@ -151,7 +154,7 @@ __device__ __forceinline__ int producer_preissue(DrSmem &sm, const CUtensorMap *
 {
     int n = 0;
     TileWalk tw;
-    tw.init(n_units, p.n_row_tiles);
+    tw.init(n_units, p.n_strips);
     while (n < kStages && tw.next()) {
         issue_tile(sm, tmc, tms, tmt, n, tw.rt(), tw.st());
         ++n;
@@ -164,7 +167,7 @@ __device__ __forceinline__ int producer_loop(DrSmem &sm, const CUtensorMap *tmc,
 {
     int issued = pre;
     TileWalk tw;
-    tw.init(n_units, p.n_row_tiles);
+    tw.init(n_units, p.n_strips);
     for (int it = 0; tw.next(); ++it) {
         const int rt = tw.rt(), st = tw.st();
         const int s = it % kStages;
@@ -277,11 +280,12 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
         const float4 t4 = tp[i >> 1];
         const float2 qa = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i][c]));
         const float2 qb = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i + 1][c]));
-        // decoded values are exact products; len = 1 butterflies
+        // len = 1 butterflies on the decoded values, which are exact products:
+        // one rounding each, fl(da + qb tb) and fl(da - qb tb), as a fused
+        // multiply-add with the exact product qb tb gives
         const float2 da = mul2(qa, make_float2(t4.x, t4.y));
-        const float2 db = mul2(qb, make_float2(t4.z, t4.w));
-        u[i] = add2(da, db);
-        u[i + 1] = sub2(da, db);
+        u[i] = __ffma2_rn(qb, make_float2(t4.z, t4.w), da);
+        u[i + 1] = __ffma2_rn(qb, make_float2(-t4.z, -t4.w), da);
     }
     // remaining Walsh-Hadamard butterflies, len = 2, 4, 8
 #pragma unroll
@@ -295,11 +299,11 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
             u[a + len] = sub2(x, y);
         }
     }
-    float b0 = 0.0f, b1 = 0.0f;
+    float b0 = fmaxf(fabsf(u[0].x), fabsf(u[1].x)), b1 = fmaxf(fabsf(u[0].y), fabsf(u[1].y));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        b0 = fmaxf(b0, fabsf(u[i].x));
-        b1 = fmaxf(b1, fabsf(u[i].y));
+    for (int i = 2; i < 16; i += 2) {
+        b0 = max3_abs(b0, u[i].x, u[i + 1].x);
+        b1 = max3_abs(b1, u[i].y, u[i + 1].y);
     }
     s2 = cvt_e4m3x2(b0 * ce, b1 * ce);
     const float2 r2 = make_float2(rtab[s2 & 0xffu], rtab[(s2 >> 8) & 0xffu]);
@@ -309,8 +313,8 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
     if (kSR) {
         // row i of the block takes random byte i of its column's 16 bytes
         const uint64_t pos = (uint64_t)m.off * (uint64_t)p.H + (uint64_t)h0 * (uint64_t)m.n + (uint64_t)(rl + r0);
-        const Philox4 ra = sr_bytes16(p.seed, 1u, pos);
-        const Philox4 rb = sr_bytes16(p.seed, 1u, pos + (uint64_t)m.n);
+        const Philox4 ra = sr_bytes16(p.key, 1u, pos);
+        const Philox4 rb = sr_bytes16(p.key, 1u, pos + (uint64_t)m.n);
         cw0 = make_uint2(cvt_e2m1x8_sr(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x, ra.x, ra.y),
                          cvt_e2m1x8_sr(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x, ra.z,
                                        ra.w));
@@ -326,7 +330,8 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
 }
 
 template <bool kSR>
-__device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_rw, const DrArgs &p, int n_units)
+__device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_rw, const CUtensorMap *tm_rws,
+                                             const DrArgs &p, int n_units)
 {
     const int c = threadIdx.x;          // 0 .. kConsumers-1
     const int warp = c >> 5, lane = c & 31;
@@ -338,7 +343,7 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
     int done = 0;
     int cur_e = -1;   // expert whose S_enc / s table this warp holds
     TileWalk tw;
-    tw.init(n_units, p.n_row_tiles);
+    tw.init(n_units, p.n_strips);
     for (int it = 0; tw.next(); ++it) {
         const int rt = tw.rt(), st = tw.st();
         const int s = it % kStages;
@@ -358,14 +363,14 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
         if (p.do_rowwise && c < kTileRows) {
             if (c == 0) {
                 tma_store_2d(tm_rw, st * kCodeBytes, row0, &sm.codes[s][0][0]);
+                if (p.rws_tma)
+                    tma_store_2d(tm_rws, st * kScaleBytes, row0, &sm.scales[s][0][0]);
                 tma_store_commit();
             }
-            const int nb = min(kScaleBytes, H / 16 - st * kScaleBytes);
-            uint8_t *dst = p.rw_scales + (int64_t)(row0 + c) * (H / 16) + st * kScaleBytes;
-            const uint8_t *src = &sm.scales[s][c][0];
-            if (nb == kScaleBytes && ((H / 16) % 16) == 0) {
-                st16g(dst, *reinterpret_cast<const uint4 *>(src));
-            } else {
+            if (!p.rws_tma) {
+                const int nb = min(kScaleBytes, H / 16 - st * kScaleBytes);
+                uint8_t *dst = p.rw_scales + (int64_t)(row0 + c) * (H / 16) + st * kScaleBytes;
+                const uint8_t *src = &sm.scales[s][c][0];
                 for (int b = 0; b < nb; b += 2)
                     *reinterpret_cast<uint16_t *>(dst + b) = *reinterpret_cast<const uint16_t *>(src + b);
             }
@@ -403,6 +408,7 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
         __syncwarp();
 
         const int h0 = st * kTileCols + 2 * pc;
+        uint32_t csc0 = 0u, csc1 = 0u;
         if (h0 < H) {
             const float2 *ctab = &tab[lane >> 3][0];
             uint8_t *d0 = p.cw_codes + (int64_t)m.off * (H / 2) + (int64_t)h0 * (m.n / 2) + (rl + 64 * hh) / 2;
@@ -431,9 +437,36 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
                 st16g(d1, q1[0]);
                 st16g(d1 + 16, q1[1]);
             }
-            uint8_t *cs = p.cw_scales + (int64_t)m.off * (H / 16) + (int64_t)h0 * (m.n / 16) + (rl + 64 * hh) / 16;
-            *reinterpret_cast<uint32_t *>(cs) = sc0;
-            *reinterpret_cast<uint32_t *>(cs + m.n / 16) = sc1;
+            // rows 64..127 hand their scale bytes to the warp holding rows
+            // 0..63 of the same columns, so each column's 8 scale bytes of
+            // the tile leave in one store (the stage's reuse orders the
+            // buffer: the producer refills stage s only after both warps
+            // released it)
+            if (hh == 1) {
+                sm.csc[s][cq][lane][0] = sc0;
+                sm.csc[s][cq][lane][1] = sc1;
+            } else {
+                csc0 = sc0;
+                csc1 = sc1;
+            }
+        }
+        if (hh == 1) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.csc_full[s][cq]);
+        } else {
+            if (!mbar_wait_bounded(&sm.csc_full[s][cq], ph)) {
+                if (lane == 0) {
+                    sm.abort_flag = 1;
+                    raise_status(p.status, kDevErrTimeout);
+                }
+                break;
+            }
+            if (h0 < H) {
+                uint8_t *cs = p.cw_scales + (int64_t)m.off * (H / 16) + (int64_t)h0 * (m.n / 16) + rl / 16;
+                *reinterpret_cast<uint2 *>(cs) = make_uint2(csc0, sm.csc[s][cq][lane][0]);
+                *reinterpret_cast<uint2 *>(cs + m.n / 16) = make_uint2(csc1, sm.csc[s][cq][lane][1]);
+            }
         }
 
         // release the stage (after the rowwise TMA store has read it)
@@ -450,11 +483,12 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
 }
 
 template <bool kSR>
-__global__ void __maxnreg__(104)
+__global__ void __launch_bounds__(kThreads, 2)
 direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
                       const __grid_constant__ CUtensorMap tm_scales,
                       const __grid_constant__ CUtensorMap tm_trailer,
-                      const __grid_constant__ CUtensorMap tm_rw, DrArgs p)
+                      const __grid_constant__ CUtensorMap tm_rw, const __grid_constant__ CUtensorMap tm_rws,
+                      const __grid_constant__ DrArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
     DrSmem &sm = *reinterpret_cast<DrSmem *>(
@@ -464,6 +498,8 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], kConsumerWarps);
+            for (int q = 0; q < kConsumerWarps / 2; ++q)
+                mbar_init(&sm.csc_full[i][q], 1);
         }
         sm.abort_flag = 0;
         sm.consumed = 0;
@@ -490,8 +526,7 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
             raise_status(p.status, kDevErrCapacity);
         R = p.R_cap;
     }
-    p.n_row_tiles = R / kTileRows;
-    const int n_units = p.n_row_tiles * p.n_strips;
+    const int n_units = (R / kTileRows) * p.n_strips;
 
     const int pre = tile_prologue(sm, p, n_units, &tm_codes, &tm_scales, &tm_trailer);
 
@@ -500,7 +535,7 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         if (lane == 0)
             issued = producer_loop(sm, &tm_codes, &tm_scales, &tm_trailer, p, n_units, pre);
     } else {
-        const int done = consumer_loop<kSR>(sm, &tm_rw, p, n_units);
+        const int done = consumer_loop<kSR>(sm, &tm_rw, &tm_rws, p, n_units);
         if (threadIdx.x == 0)
             sm.consumed = done;
     }
@@ -556,8 +591,9 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     if (err != cudaSuccess || R_cap < kTileRows)   // fewer than 128 rows of capacity: no tile can exist
         return err;
 
-    CUtensorMap tm_codes, tm_scales, tm_trailer, tm_rw;
+    CUtensorMap tm_codes, tm_scales, tm_trailer, tm_rw, tm_rws;
     memset(&tm_rw, 0, sizeof(tm_rw));
+    memset(&tm_rws, 0, sizeof(tm_rws));
     const uint64_t rc = (uint64_t)R_cap;
     if (!make_map(&tm_codes, rows, (uint64_t)H / 2, rc, (uint64_t)S, kCodeBytes, kTileRows) ||
         !make_map(&tm_scales, rows + H / 2, (uint64_t)H / 16, rc, (uint64_t)S, kScaleBytes, kTileRows) ||
@@ -566,6 +602,10 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     const int do_rw = out.rw_codes != nullptr;
     if (do_rw && !make_map(&tm_rw, out.rw_codes, (uint64_t)H / 2, rc, (uint64_t)H / 2, kCodeBytes, kTileRows))
         return cudaErrorInvalidValue;
+    // rowwise scales by TMA when every strip is a whole 16-byte box and the
+    // row pitch H/16 is a multiple of 16 bytes
+    const int rws_tma = do_rw && H % kTileCols == 0 &&
+                        make_map(&tm_rws, out.rw_scales, (uint64_t)H / 16, rc, (uint64_t)H / 16, kScaleBytes, kTileRows);
 
     DrArgs a;
     a.rows = rows;
@@ -580,11 +620,12 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     a.cw_codes = out.cw_codes;
     a.cw_scales = out.cw_scales;
     a.scale_enc = out.scale_enc;
-    a.seed = seed;
+    a.key = philox_key(seed);
     a.sign_mask = sign_mask;
     a.status = status;
     a.do_rowwise = do_rw;
     a.cw_v8 = (reinterpret_cast<uintptr_t>(out.cw_codes) & 31u) == 0;
+    a.rws_tma = rws_tma;
 
     const size_t smem = sizeof(DrSmem) + 1024;
     static int done_rn[2] = {0, 0}, done_sr[2] = {0, 0};
@@ -600,9 +641,9 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
         grid = 1;
     if (rounding == 1)
         return launch_pdl(direct_receive_kernel<true>, dim3((unsigned)grid), dim3(kThreads), smem, c.stream,
-                          tm_codes, tm_scales, tm_trailer, tm_rw, a);
+                          tm_codes, tm_scales, tm_trailer, tm_rw, tm_rws, a);
     return launch_pdl(direct_receive_kernel<false>, dim3((unsigned)grid), dim3(kThreads), smem, c.stream, tm_codes,
-                      tm_scales, tm_trailer, tm_rw, a);
+                      tm_scales, tm_trailer, tm_rw, tm_rws, a);
 }
 
 } // namespace epq
