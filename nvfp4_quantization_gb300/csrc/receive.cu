@@ -17,7 +17,8 @@
 // Two launches.  expert_amax_kernel reduces each expert's 4-byte token
 // amaxes from the row trailers (the rows' data is not read) into the expert's
 // metadata and encode scale S_enc.  The tile kernel, launched behind it with
-// programmatic dependent launch, reads the offsets and S_enc once per CTA.
+// programmatic dependent launch, starts its first tile loads while the amax
+// kernel runs and reads S_enc once per CTA after waiting for it.
 //
 // Producer warp: streams tiles into a 3-stage shared-memory ring with 2-D TMA
 // loads (codes 128 B x 128 rows, scales 16 B x 128, row trailers 16 B x 128);
@@ -205,8 +206,9 @@ expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *_
                    float *__restrict__ scale_enc)
 {
     __shared__ uint32_t red[kAmaxThreads / 32];
-    pdl_launch_dependents();
     pdl_wait();
+    // the tile kernel may start now: the rows it reads are complete
+    pdl_launch_dependents();
     const int tid = threadIdx.x;
     const uint8_t *amax_at = rows + S - 12;   // A_t inside each row's trailer
     for (int e = blockIdx.x; e < E; e += gridDim.x) {
@@ -241,8 +243,7 @@ expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *_
     }
 }
 
-// Tile-kernel set-up after the wait on the amax kernel (expert offsets and
-// S_enc of every expert are in shared memory): the first tile loads.
+// Tile-kernel set-up (expert offsets in shared memory): the first tile loads.
 __device__ __forceinline__ int tile_prologue(DrSmem &sm, const DrArgs &p, int n_units, const CUtensorMap *tmc,
                                              const CUtensorMap *tms, const CUtensorMap *tmt)
 {
@@ -512,13 +513,13 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
     __syncthreads();
     pdl_launch_dependents();
-    pdl_wait();
 
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+    // The rows and the offsets were complete before this grid could start
+    // (expert_amax_kernel lets it launch only after its own wait on the pack
+    // has returned), so the first tile loads go out before the wait on the
+    // amax kernel; only S_enc comes from it.
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x)
         sm.offs[i] = __ldg(p.offsets + i);
-        if (i < p.E)
-            sm.se_cache[i] = p.scale_enc[i];
-    }
     __syncthreads();
     int R = sm.offs[p.E];
     if (R > p.R_cap) {
@@ -529,6 +530,10 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const int n_units = (R / kTileRows) * p.n_strips;
 
     const int pre = tile_prologue(sm, p, n_units, &tm_codes, &tm_scales, &tm_trailer);
+    pdl_wait();
+    for (int i = threadIdx.x; i < p.E; i += blockDim.x)
+        sm.se_cache[i] = p.scale_enc[i];
+    __syncthreads();
 
     int issued = 0;
     if (warp == kConsumerWarps) {
