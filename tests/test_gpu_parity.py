@@ -233,3 +233,24 @@ def test_route_plan_general_paths(T, E, k):
     assert_bytes_equal(plan.counts.cpu().numpy(), cnt, "counts")
     assert_bytes_equal(plan.dest.cpu().numpy()[: T * k], dest, "dest")
     assert int(plan.status.item()) == st == 0
+
+
+@pytest.mark.parametrize("T,E,k", [(1025, 8, 3), (2048, 128, 8), (1000, 256, 5), (8192, 32, 2), (4097, 64, 1)])
+def test_route_plan_small_batch_shapes(T, E, k):
+    """Routing across 512-token chunk boundaries for several k (1 to 8) and
+    up to 256 experts, with dropped, out-of-range and repeated ids."""
+    rng = np.random.default_rng(T * 7 + k)
+    topk = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    topk[rng.random((T, k)) < 0.03] = -1
+    bad = rng.random((T, k)) < 0.002
+    topk[bad] = E + 3
+    if k > 1:
+        rep = rng.random(T) < 0.01
+        topk[rep, 1] = topk[rep, 0]
+    off, cnt, dest, st = oracle.route_plan(topk, E, 128)
+    plan = nq.ep_route_plan(torch.from_numpy(topk).cuda(), E, 128)
+    torch.cuda.synchronize()
+    assert_bytes_equal(plan.offsets.cpu().numpy(), off, "offsets")
+    assert_bytes_equal(plan.counts.cpu().numpy(), cnt, "counts")
+    assert_bytes_equal(plan.dest.cpu().numpy()[: T * k], dest, "dest")
+    assert int(plan.status.item()) == st
