@@ -407,7 +407,11 @@ __device__ __forceinline__ void encode_lane_blocks(const uint32_t (&w)[NB][8], c
 // and stores them to every destination row.  CTAs past the token CTAs write
 // the padding rows.
 constexpr int kPackWarps = 4;
-constexpr int kBuf = 2;
+// One buffer per warp: the next token's copy is issued as soon as the current
+// one is in registers, so it overlaps the encode and the stores; a second
+// buffer bought nothing but shared memory (it capped residency at one CTA per
+// SM at H = 7168, three at H = 4096).
+constexpr int kBuf = 1;
 
 template <int NB, bool kSR>
 __global__ void __launch_bounds__(32 * kPackWarps)

@@ -300,12 +300,14 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
             u[a + len] = sub2(x, y);
         }
     }
-    float b0 = fmaxf(fabsf(u[0].x), fabsf(u[1].x)), b1 = fmaxf(fabsf(u[0].y), fabsf(u[1].y));
-#pragma unroll
-    for (int i = 2; i < 16; i += 2) {
-        b0 = max3_abs(b0, u[i].x, u[i + 1].x);
-        b1 = max3_abs(b1, u[i].y, u[i + 1].y);
-    }
+    // block maxima as a tree of 3-input maxima (depth 3, not a chain of 7)
+    const float p0 = max3_abs(fabsf(u[0].x), u[1].x, u[2].x), q0 = max3_abs(fabsf(u[0].y), u[1].y, u[2].y);
+    const float p1 = max3_abs(fabsf(u[3].x), u[4].x, u[5].x), q1 = max3_abs(fabsf(u[3].y), u[4].y, u[5].y);
+    const float p2 = max3_abs(fabsf(u[6].x), u[7].x, u[8].x), q2 = max3_abs(fabsf(u[6].y), u[7].y, u[8].y);
+    const float p3 = max3_abs(fabsf(u[9].x), u[10].x, u[11].x), q3 = max3_abs(fabsf(u[9].y), u[10].y, u[11].y);
+    const float p4 = max3_abs(fabsf(u[12].x), u[13].x, u[14].x), q4 = max3_abs(fabsf(u[12].y), u[13].y, u[14].y);
+    const float b0 = fmaxf(fmaxf(p0, p1), max3_abs(fmaxf(p2, p3), p4, u[15].x));
+    const float b1 = fmaxf(fmaxf(q0, q1), max3_abs(fmaxf(q2, q3), q4, u[15].y));
     s2 = cvt_e4m3x2(b0 * ce, b1 * ce);
     const float2 r2 = make_float2(rtab[s2 & 0xffu], rtab[(s2 >> 8) & 0xffu]);
 #pragma unroll
