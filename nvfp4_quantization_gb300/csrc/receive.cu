@@ -38,6 +38,7 @@
 // holding rows 0..63 so each column's 8 scale bytes leave in one store.
 #include <cudaTypedefs.h>
 #include <float.h>
+#include <math.h>
 #include <string.h>
 
 #include "epq_device.cuh"
@@ -69,6 +70,7 @@ struct __align__(128) DrSmem {
     uint32_t trailer[kStages][kTileRows][4];
     float2 wtab[kConsumerWarps][4][kWTabStride]; // per warp: [column block][row] decode scale, twice
     float wrtab[kConsumerWarps][128];           // per warp: [E4M3 code s] -> fl32(S_enc / s) of its expert
+    float rcp[128];                             // [E4M3 code s] -> RN(1 / s), 0 for s = 0
     uint32_t csc[kStages][kConsumerWarps / 2][32][2]; // [stage][column quarter][lane]: scales of rows 64..127
     StageMeta meta[kStages];
     float se_cache[kMaxExperts];                // S_enc of the experts this CTA meets
@@ -101,6 +103,7 @@ struct DrArgs {
     uint32_t *status;
     int do_rowwise;
     int cw_v8;         // cw_codes is 32-byte aligned: 32-byte stores
+    float rcp[128];    // RN(1 / s) for every E4M3 code s (0 for s = 0), computed on the host
     int rws_tma;       // rowwise scales leave by TMA store (H % 256 == 0)
 };
 
@@ -268,7 +271,7 @@ __device__ __forceinline__ void st32g(void *p, uint4 a, uint4 b)
 // One 16-row block of the thread's two columns: decode, RHT, block scales,
 // E2M1 codes.  Returns the 8 code bytes of each column (cw0, cw1) and the two
 // E4M3 scale codes (s2: column 0 in the low byte).
-template <bool kSR>
+template <bool kSR, bool kFastR>
 __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 *tab, const float *rtab, int c,
                                           int r0, float ce, const DrArgs &p, const StageMeta &m, int h0, int rl,
                                           uint2 &cw0, uint2 &cw1, uint32_t &s2)
@@ -309,7 +312,21 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
     const float b0 = fmaxf(fmaxf(p0, p1), max3_abs(fmaxf(p2, p3), p4, u[15].x));
     const float b1 = fmaxf(fmaxf(q0, q1), max3_abs(fmaxf(q2, q3), q4, u[15].y));
     s2 = cvt_e4m3x2(b0 * ce, b1 * ce);
-    const float2 r2 = make_float2(rtab[s2 & 0xffu], rtab[(s2 >> 8) & 0xffu]);
+    float2 r2;
+    if (kFastR) {
+        // r = fl32(S_enc / s) by one Markstein step from y = RN(1/s): q = RN(S_enc y),
+        // e = S_enc - s q (exact), r = RN(q + e y) is the correctly rounded
+        // quotient (S_enc within 2^(+-100): nothing overflows or underflows);
+        // s = 0 gives y = 0 and r = 0
+        const float2 y2 = make_float2(sm.rcp[s2 & 0xffu], sm.rcp[(s2 >> 8) & 0xffu]);
+        const float2 sv = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(s2 & 0xffffu));
+        const float2 se2 = make_float2(m.se, m.se);
+        const float2 q = mul2(se2, y2);
+        const float2 e = __ffma2_rn(make_float2(-sv.x, -sv.y), q, se2);
+        r2 = __ffma2_rn(e, y2, q);
+    } else {
+        r2 = make_float2(rtab[s2 & 0xffu], rtab[(s2 >> 8) & 0xffu]);
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i)
         u[i] = mul2(u[i], r2);
@@ -399,7 +416,10 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
             tab[3][rloc] = make_float2(v3, v3);
         }
         const float *rtab = sm.wrtab[warp];
-        if (m.e != cur_e) {
+        // S_enc / s by a Markstein step when S_enc is in range, else from this
+        // warp's table of the expert's 128 quotients
+        const bool fast_r = m.se >= 0x1p-100f && m.se <= 0x1p100f;
+        if (!fast_r && m.e != cur_e) {
             cur_e = m.e;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -423,8 +443,15 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
                 uint2 a0, a1, b0, b1;
                 uint32_t s2a, s2b;
                 const int r0 = 64 * hh + 32 * bp;
-                rht_block<kSR>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, p, m, h0, rl, a0, a1, s2a);
-                rht_block<kSR>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, p, m, h0, rl, b0, b1, s2b);
+                if (fast_r) {
+                    rht_block<kSR, true>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, p, m, h0, rl, a0, a1, s2a);
+                    rht_block<kSR, true>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, p, m, h0, rl, b0, b1,
+                                         s2b);
+                } else {
+                    rht_block<kSR, false>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, p, m, h0, rl, a0, a1, s2a);
+                    rht_block<kSR, false>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, p, m, h0, rl, b0, b1,
+                                          s2b);
+                }
                 q0[bp] = make_uint4(a0.x, a0.y, b0.x, b0.y);
                 q1[bp] = make_uint4(a1.x, a1.y, b1.x, b1.y);
                 sc0 |= ((s2a & 0xffu) | ((s2b & 0xffu) << 8)) << (16 * bp);
@@ -522,6 +549,8 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     // amax kernel; only S_enc comes from it.
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x)
         sm.offs[i] = __ldg(p.offsets + i);
+    for (int i = threadIdx.x; i < 128; i += blockDim.x)
+        sm.rcp[i] = p.rcp[i];
     __syncthreads();
     int R = sm.offs[p.E];
     if (R > p.R_cap) {
@@ -633,6 +662,11 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     a.do_rowwise = do_rw;
     a.cw_v8 = (reinterpret_cast<uintptr_t>(out.cw_codes) & 31u) == 0;
     a.rws_tma = rws_tma;
+    for (int code = 0; code < 128; ++code) {
+        const int ex = code >> 3, mt = code & 7;
+        const float v = ex == 0 ? (float)mt * (1.0f / 512.0f) : (1.0f + (float)mt / 8.0f) * ldexpf(1.0f, ex - 7);
+        a.rcp[code] = (v == 0.0f || code == 127) ? 0.0f : 1.0f / v;   // IEEE single division: RN(1/v)
+    }
 
     const size_t smem = sizeof(DrSmem) + 1024;
     static int done_rn[2] = {0, 0}, done_sr[2] = {0, 0};
