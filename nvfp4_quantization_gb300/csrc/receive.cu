@@ -20,12 +20,13 @@
 // programmatic dependent launch, starts its first tile loads while the amax
 // kernel runs and reads S_enc once per CTA after waiting for it.
 //
-// Producer warp: streams tiles into a 3-stage shared-memory ring with 2-D TMA
-// loads (codes 128 B x 128 rows, scales 16 B x 128, row trailers 16 B x 128);
-// the tile's expert, offsets and S_enc go into the stage before the stage's
-// barrier is released.
+// Stages: a 3-stage shared-memory ring of tiles loaded by 2-D TMA (codes 128 B
+// x 128 rows, scales 16 B x 128, row trailers 16 B x 128).  There is no
+// producer warp: thread 0 issues the first tiles' loads, and the last warp to
+// finish with a stage (an acquire-release counter) writes the metadata of the
+// tile kStages ahead (expert, its offsets, S_enc) and issues its loads.
 //
-// Consumer warps (8): the rowwise operand leaves straight from the ring (TMA
+// Warps (8): the rowwise operand leaves straight from the ring (TMA
 // stores of the codes and, when H % 256 == 0, of the scales; the token scale
 // by threads).  For the columnwise operand each thread owns two adjacent
 // hidden columns (one code byte per row) and 64 of the 128 rows: it decodes
@@ -53,7 +54,7 @@ constexpr int kScaleBytes = kTileCols / 16;  // 16
 constexpr int kStages = 3;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kThreads = kConsumers + 32;    // + 1 producer warp
+constexpr int kThreads = kConsumers;         // no producer warp: the last warp to free a stage refills it
 constexpr uint32_t kStageTx = kTileRows * (kCodeBytes + kScaleBytes + 16);
 constexpr int kWarpRows = kTileRows / 2;     // rows of a tile one consumer warp handles
 constexpr int kWTabStride = kWarpRows + 2;   // float2 entries; pad: a warp's 4 column blocks hit distinct banks
@@ -73,13 +74,15 @@ struct __align__(128) DrSmem {
     float rcp[128];                             // [E4M3 code s] -> RN(1 / s), 0 for s = 0
     uint32_t csc[kStages][kConsumerWarps / 2][32][2]; // [stage][column quarter][lane]: scales of rows 64..127
     StageMeta meta[kStages];
-    float se_cache[kMaxExperts];                // S_enc of the experts this CTA meets
+    float se_cache[kMaxExperts];                // S_enc of every expert
+    float ce_cache[kMaxExperts];                // fl32(S_enc / 6) of every expert
     int offs[kMaxExperts + 1];                  // expert_offsets, copied once
     uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint32_t rel[kStages];                      // warps done with the stage's current tile
     uint64_t csc_full[kStages][kConsumerWarps / 2];   // csc[stage][quarter] written
     int abort_flag;
-    int consumed;
+    int consumed;                               // fewest tiles any warp finished
+    int issued;                                 // tiles whose loads were issued
 };
 
 // two CTAs per SM: each gets at most (228 KB - 2 x 1 KB reserved) / 2
@@ -107,25 +110,12 @@ struct DrArgs {
     int rws_tma;       // rowwise scales leave by TMA store (H % 256 == 0)
 };
 
-// Tiles of this CTA: u = blockIdx.x + k * gridDim.x, k = 0, 1, ... over the
-// tiles numbered row-major (u = row_tile * n_strips + strip).  At any moment
-// the grid works on one contiguous band of row tiles, all strips of each:
-// complete rowwise rows and, because expert slots are contiguous row ranges,
-// whole columnwise column runs are written within a short window, so the
-// output reaches DRAM in whole pages instead of scattered lines.
-struct TileWalk {
-    int u, n, ns;
-    __device__ __forceinline__ void init(int n_units, int n_strips)
-    {
-        u = (int)blockIdx.x - (int)gridDim.x;
-        n = n_units;
-        ns = n_strips;
-    }
-    // Advance to the next tile; false when the CTA's share is exhausted.
-    __device__ __forceinline__ bool next() { return (u += (int)gridDim.x) < n; }
-    __device__ __forceinline__ int rt() const { return u / ns; }
-    __device__ __forceinline__ int st() const { return u % ns; }
-};
+// Tiles of a CTA: u = blockIdx.x + k * gridDim.x, k = 0, 1, ... over the tiles
+// numbered row-major (u = row_tile * n_strips + strip).  At any moment the grid
+// works on one contiguous band of row tiles, all strips of each: complete
+// rowwise rows and, because expert slots are contiguous row ranges, whole
+// columnwise column runs are written within a short window, so the output
+// reaches DRAM in whole pages instead of scattered lines.
 
 // Last e with offs[e] <= row (offs in shared memory).
 __device__ __forceinline__ int expert_of_row(const int *offs, int E, int row)
@@ -141,7 +131,8 @@ __device__ __forceinline__ int expert_of_row(const int *offs, int E, int row)
     return lo;
 }
 
-// Issue the TMA loads of the it-th tile into its stage (lane 0 only).
+// Issue the TMA loads of a tile into stage s, expecting their bytes on the
+// stage's barrier (one thread).
 __device__ __forceinline__ void issue_tile(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
                                            const CUtensorMap *tmt, int s, int rt, int st)
 {
@@ -152,49 +143,23 @@ __device__ __forceinline__ void issue_tile(DrSmem &sm, const CUtensorMap *tmc, c
     tma_load_2d(&sm.trailer[s][0][0], tmt, 0, row0, &sm.full[s]);
 }
 
-// First min(kStages, tiles) loads: go out before the prologue.
-__device__ __forceinline__ int producer_preissue(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
-                                                 const CUtensorMap *tmt, const DrArgs &p, int n_units)
+// The tile this CTA takes it-th; false past the CTA's share.
+__device__ __forceinline__ bool tile_of(const DrArgs &p, int n_units, int it, int &rt, int &st)
 {
-    int n = 0;
-    TileWalk tw;
-    tw.init(n_units, p.n_strips);
-    while (n < kStages && tw.next()) {
-        issue_tile(sm, tmc, tms, tmt, n, tw.rt(), tw.st());
-        ++n;
-    }
-    return n;
+    const int u = (int)blockIdx.x + it * (int)gridDim.x;
+    if (u >= n_units)
+        return false;
+    rt = u / p.n_strips;
+    st = u % p.n_strips;
+    return true;
 }
 
-__device__ __forceinline__ int producer_loop(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
-                                             const CUtensorMap *tmt, const DrArgs &p, int n_units, int pre)
+// The stage's tile metadata: expert, its slot, S_enc and S_enc / 6.
+__device__ __forceinline__ void stage_meta(DrSmem &sm, const DrArgs &p, int s, int rt)
 {
-    int issued = pre;
-    TileWalk tw;
-    tw.init(n_units, p.n_strips);
-    for (int it = 0; tw.next(); ++it) {
-        const int rt = tw.rt(), st = tw.st();
-        const int s = it % kStages;
-        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-        if (it >= pre) {
-            const bool ok = mbar_wait_bounded(&sm.empty[s], ph ^ 1u);
-            if (!ok)
-                raise_status(p.status, kDevErrTimeout);
-            if (!ok || sm.abort_flag) {
-                sm.abort_flag = 1;
-                break;
-            }
-            issue_tile(sm, tmc, tms, tmt, s, rt, st);
-            issued = it + 1;
-        }
-        const int e = expert_of_row(sm.offs, p.E, rt * kTileRows);
-        const int off = sm.offs[e];
-        const int n = sm.offs[e + 1] - off;
-        const float se = sm.se_cache[e];
-        sm.meta[s] = StageMeta{e, off, n, se, __fdiv_rn(se, 6.0f)};
-        mbar_arrive(&sm.full[s]); // releases the metadata with the stage
-    }
-    return issued;
+    const int e = expert_of_row(sm.offs, p.E, rt * kTileRows);
+    const int off = sm.offs[e];
+    sm.meta[s] = StageMeta{e, off, sm.offs[e + 1] - off, sm.se_cache[e], sm.ce_cache[e]};
 }
 
 // Per-expert metadata (one CTA per expert, grid-stride): the rowwise amax is
@@ -246,11 +211,17 @@ expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *_
     }
 }
 
-// Tile-kernel set-up (expert offsets in shared memory): the first tile loads.
+// Tile-kernel set-up (expert offsets in shared memory; thread 0): the loads of
+// the first min(kStages, tiles) tiles, before S_enc is known.
 __device__ __forceinline__ int tile_prologue(DrSmem &sm, const DrArgs &p, int n_units, const CUtensorMap *tmc,
                                              const CUtensorMap *tms, const CUtensorMap *tmt)
 {
-    return threadIdx.x == kConsumers ? producer_preissue(sm, tmc, tms, tmt, p, n_units) : 0;
+    int n = 0, rt, st;
+    while (n < kStages && tile_of(p, n_units, n, rt, st)) {
+        issue_tile(sm, tmc, tms, tmt, n, rt, st);
+        ++n;
+    }
+    return n;
 }
 
 __device__ __forceinline__ void st16g(void *p, uint4 v)
@@ -351,7 +322,8 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
 
 template <bool kSR>
 __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_rw, const CUtensorMap *tm_rws,
-                                             const DrArgs &p, int n_units)
+                                             const CUtensorMap *tmc, const CUtensorMap *tms,
+                                             const CUtensorMap *tmt, const DrArgs &p, int n_units)
 {
     const int c = threadIdx.x;          // 0 .. kConsumers-1
     const int warp = c >> 5, lane = c & 31;
@@ -362,10 +334,8 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
     float2(*tab)[kWTabStride] = sm.wtab[warp];
     int done = 0;
     int cur_e = -1;   // expert whose S_enc / s table this warp holds
-    TileWalk tw;
-    tw.init(n_units, p.n_strips);
-    for (int it = 0; tw.next(); ++it) {
-        const int rt = tw.rt(), st = tw.st();
+    int rt, st;
+    for (int it = 0; tile_of(p, n_units, it, rt, st); ++it) {
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
         if (!mbar_wait_bounded(&sm.full[s], ph) || sm.abort_flag) {
@@ -499,12 +469,30 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
             }
         }
 
-        // release the stage (after the rowwise TMA store has read it)
+        // release the stage (after the rowwise TMA store has read it); the
+        // last warp to release it refills it with the tile kStages ahead
         if (c == 0 && p.do_rowwise)
             tma_store_wait_read0();
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&sm.empty[s]);
+        if (lane == 0) {
+            uint32_t before;
+            asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                         : "=r"(before)
+                         : "r"((uint32_t)__cvta_generic_to_shared(&sm.rel[s]))
+                         : "memory");
+            if (before == kConsumerWarps - 1) {
+                sm.rel[s] = 0u;
+                int rt2, st2;
+                if (tile_of(p, n_units, it + kStages, rt2, st2)) {
+                    stage_meta(sm, p, s, rt2);
+                    // bytes expected before the arrival, so the phase waits for them;
+                    // the arrival releases the metadata
+                    issue_tile(sm, tmc, tms, tmt, s, rt2, st2);
+                    mbar_arrive(&sm.full[s]);
+                    atomicAdd(&sm.issued, 1);
+                }
+            }
+        }
         done = it + 1;
     }
     if (c == 0 && p.do_rowwise)
@@ -523,19 +511,17 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     extern __shared__ uint8_t smem_raw[];
     DrSmem &sm = *reinterpret_cast<DrSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], kConsumerWarps);
+            sm.rel[i] = 0u;
             for (int q = 0; q < kConsumerWarps / 2; ++q)
                 mbar_init(&sm.csc_full[i][q], 1);
         }
         sm.abort_flag = 0;
-        sm.consumed = 0;
+        sm.consumed = 0x7fffffff;
         fence_mbar_init();
-    }
-    if (warp == kConsumerWarps && lane == 0) {
         tma_prefetch_desc(&tm_codes);
         tma_prefetch_desc(&tm_scales);
         tma_prefetch_desc(&tm_trailer);
@@ -560,27 +546,33 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
     const int n_units = (R / kTileRows) * p.n_strips;
 
-    const int pre = tile_prologue(sm, p, n_units, &tm_codes, &tm_scales, &tm_trailer);
+    const int pre = threadIdx.x == 0 ? tile_prologue(sm, p, n_units, &tm_codes, &tm_scales, &tm_trailer) : 0;
     pdl_wait();
-    for (int i = threadIdx.x; i < p.E; i += blockDim.x)
-        sm.se_cache[i] = p.scale_enc[i];
-    __syncthreads();
-
-    int issued = 0;
-    if (warp == kConsumerWarps) {
-        if (lane == 0)
-            issued = producer_loop(sm, &tm_codes, &tm_scales, &tm_trailer, p, n_units, pre);
-    } else {
-        const int done = consumer_loop<kSR>(sm, &tm_rw, &tm_rws, p, n_units);
-        if (threadIdx.x == 0)
-            sm.consumed = done;
+    for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
+        const float se = p.scale_enc[i];
+        sm.se_cache[i] = se;
+        sm.ce_cache[i] = __fdiv_rn(se, 6.0f);
     }
     __syncthreads();
-    // after an abort warps may have consumed different numbers of tiles
-    
-    // never leave with a tile load still in flight (only after an abort)
-    if (warp == kConsumerWarps && lane == 0) {
-        for (int i = sm.consumed; i < issued; ++i)
+    if (threadIdx.x == 0) {
+        // metadata of the preissued tiles; the arrivals release it
+        for (int it = 0; it < pre; ++it) {
+            int rt, st;
+            (void)tile_of(p, n_units, it, rt, st);
+            stage_meta(sm, p, it, rt);
+            mbar_arrive(&sm.full[it]);
+        }
+        sm.issued = pre;
+    }
+
+    const int done = consumer_loop<kSR>(sm, &tm_rw, &tm_rws, &tm_codes, &tm_scales, &tm_trailer, p, n_units);
+    if (lane == 0)
+        atomicMin(&sm.consumed, done);
+    __syncthreads();
+    // never leave with a tile load still in flight (only after an abort, when
+    // warps may have stopped at different tiles)
+    if (threadIdx.x == 0) {
+        for (int i = sm.consumed; i < sm.issued; ++i)
             (void)mbar_wait_bounded(&sm.full[i % kStages], (uint32_t)(i / kStages) & 1u);
     }
 }
