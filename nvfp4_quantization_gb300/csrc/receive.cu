@@ -20,7 +20,8 @@
 // programmatic dependent launch, starts its first tile loads while the amax
 // kernel runs and reads S_enc once per CTA after waiting for it.
 //
-// Stages: a 3-stage shared-memory ring of tiles loaded by 2-D TMA (codes 128 B
+// Stages: a shared-memory ring of tiles (2 stages and 3 CTAs per SM for RNE,
+// 3 stages and 2 CTAs per SM for SR) loaded by 2-D TMA (codes 128 B
 // x 128 rows, scales 16 B x 128, row trailers 16 B x 128).  There is no
 // producer warp: thread 0 issues the first tiles' loads, and the last warp to
 // finish with a stage (an acquire-release counter) writes the metadata of the
@@ -51,7 +52,6 @@ constexpr int kTileRows = 128;
 constexpr int kTileCols = 256;
 constexpr int kCodeBytes = kTileCols / 2;    // 128
 constexpr int kScaleBytes = kTileCols / 16;  // 16
-constexpr int kStages = 3;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers;         // no producer warp: the last warp to free a stage refills it
@@ -65,28 +65,39 @@ struct StageMeta {
     float se, ce;        // S_enc and fl32(S_enc / 6)
 };
 
+template <int NS>   // ring stages
 struct __align__(128) DrSmem {
-    uint8_t codes[kStages][kTileRows][kCodeBytes];
-    uint8_t scales[kStages][kTileRows][kScaleBytes];
-    uint32_t trailer[kStages][kTileRows][4];
+    static constexpr int kNS = NS;
+    uint8_t codes[NS][kTileRows][kCodeBytes];
+    uint8_t scales[NS][kTileRows][kScaleBytes];
+    uint32_t trailer[NS][kTileRows][4];
     float2 wtab[kConsumerWarps][4][kWTabStride]; // per warp: [column block][row] decode scale, twice
     float wrtab[kConsumerWarps][128];           // per warp: [E4M3 code s] -> fl32(S_enc / s) of its expert
     float rcp[128];                             // [E4M3 code s] -> RN(1 / s), 0 for s = 0
-    uint32_t csc[kStages][kConsumerWarps / 2][32][2]; // [stage][column quarter][lane]: scales of rows 64..127
-    StageMeta meta[kStages];
+    uint32_t csc[NS][kConsumerWarps / 2][32][2]; // [stage][column quarter][lane]: scales of rows 64..127
+    StageMeta meta[NS];
     float se_cache[kMaxExperts];                // S_enc of every expert
-    float ce_cache[kMaxExperts];                // fl32(S_enc / 6) of every expert
     int offs[kMaxExperts + 1];                  // expert_offsets, copied once
-    uint64_t full[kStages];
-    uint32_t rel[kStages];                      // warps done with the stage's current tile
-    uint64_t csc_full[kStages][kConsumerWarps / 2];   // csc[stage][quarter] written
+    uint64_t full[NS];
+    uint32_t rel[NS];                      // warps done with the stage's current tile
+    uint64_t csc_full[NS][kConsumerWarps / 2];   // csc[stage][quarter] written
     int abort_flag;
     int consumed;                               // fewest tiles any warp finished
     int issued;                                 // tiles whose loads were issued
 };
 
 // two CTAs per SM: each gets at most (228 KB - 2 x 1 KB reserved) / 2
-static_assert(sizeof(DrSmem) + 1024 <= 113 * 1024, "direct receive must fit two CTAs per SM");
+// RNE: two stages and three CTAs per SM (80 registers suffice); SR: three
+// stages and two CTAs per SM (the Philox state needs 128 registers)
+template <bool kSR>
+struct DrCfg {
+    static constexpr int kStages = kSR ? 3 : 2;
+    static constexpr int kCtasPerSm = kSR ? 2 : 3;
+    using Smem = DrSmem<kStages>;
+};
+// each CTA gets at most (228 KB - 1 KB reserved per CTA) / CTAs per SM
+static_assert(sizeof(DrCfg<true>::Smem) + 1024 <= 113 * 1024, "SR direct receive must fit two CTAs per SM");
+static_assert(sizeof(DrCfg<false>::Smem) + 1024 <= 75 * 1024, "RNE direct receive must fit three CTAs per SM");
 
 struct DrArgs {
     const uint8_t *rows;
@@ -133,7 +144,8 @@ __device__ __forceinline__ int expert_of_row(const int *offs, int E, int row)
 
 // Issue the TMA loads of a tile into stage s, expecting their bytes on the
 // stage's barrier (one thread).
-__device__ __forceinline__ void issue_tile(DrSmem &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
+template <class Sm>
+__device__ __forceinline__ void issue_tile(Sm &sm, const CUtensorMap *tmc, const CUtensorMap *tms,
                                            const CUtensorMap *tmt, int s, int rt, int st)
 {
     const int row0 = rt * kTileRows;
@@ -155,11 +167,13 @@ __device__ __forceinline__ bool tile_of(const DrArgs &p, int n_units, int it, in
 }
 
 // The stage's tile metadata: expert, its slot, S_enc and S_enc / 6.
-__device__ __forceinline__ void stage_meta(DrSmem &sm, const DrArgs &p, int s, int rt)
+template <class Sm>
+__device__ __forceinline__ void stage_meta(Sm &sm, const DrArgs &p, int s, int rt)
 {
     const int e = expert_of_row(sm.offs, p.E, rt * kTileRows);
     const int off = sm.offs[e];
-    sm.meta[s] = StageMeta{e, off, sm.offs[e + 1] - off, sm.se_cache[e], sm.ce_cache[e]};
+    const float se = sm.se_cache[e];
+    sm.meta[s] = StageMeta{e, off, sm.offs[e + 1] - off, se, __fdiv_rn(se, 6.0f)};
 }
 
 // Per-expert metadata (one CTA per expert, grid-stride): the rowwise amax is
@@ -213,11 +227,12 @@ expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *_
 
 // Tile-kernel set-up (expert offsets in shared memory; thread 0): the loads of
 // the first min(kStages, tiles) tiles, before S_enc is known.
-__device__ __forceinline__ int tile_prologue(DrSmem &sm, const DrArgs &p, int n_units, const CUtensorMap *tmc,
+template <class Sm>
+__device__ __forceinline__ int tile_prologue(Sm &sm, const DrArgs &p, int n_units, const CUtensorMap *tmc,
                                              const CUtensorMap *tms, const CUtensorMap *tmt)
 {
     int n = 0, rt, st;
-    while (n < kStages && tile_of(p, n_units, n, rt, st)) {
+    while (n < Sm::kNS && tile_of(p, n_units, n, rt, st)) {
         issue_tile(sm, tmc, tms, tmt, n, rt, st);
         ++n;
     }
@@ -242,8 +257,8 @@ __device__ __forceinline__ void st32g(void *p, uint4 a, uint4 b)
 // One 16-row block of the thread's two columns: decode, RHT, block scales,
 // E2M1 codes.  Returns the 8 code bytes of each column (cw0, cw1) and the two
 // E4M3 scale codes (s2: column 0 in the low byte).
-template <bool kSR, bool kFastR>
-__device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 *tab, const float *rtab, int c,
+template <bool kSR, bool kFastR, class Sm>
+__device__ __forceinline__ void rht_block(const Sm &sm, int s, const float2 *tab, const float *rtab, int c,
                                           int r0, float ce, const DrArgs &p, const StageMeta &m, int h0, int rl,
                                           uint2 &cw0, uint2 &cw1, uint32_t &s2)
 {
@@ -320,8 +335,8 @@ __device__ __forceinline__ void rht_block(const DrSmem &sm, int s, const float2 
                      cvt_e2m1x8(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y));
 }
 
-template <bool kSR>
-__device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_rw, const CUtensorMap *tm_rws,
+template <bool kSR, class Sm>
+__device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, const CUtensorMap *tm_rws,
                                              const CUtensorMap *tmc, const CUtensorMap *tms,
                                              const CUtensorMap *tmt, const DrArgs &p, int n_units)
 {
@@ -336,8 +351,8 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
     int cur_e = -1;   // expert whose S_enc / s table this warp holds
     int rt, st;
     for (int it = 0; tile_of(p, n_units, it, rt, st); ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+        const int s = it % Sm::kNS;
+        const uint32_t ph = (uint32_t)(it / Sm::kNS) & 1u;
         if (!mbar_wait_bounded(&sm.full[s], ph) || sm.abort_flag) {
             if (lane == 0) {
                 sm.abort_flag = 1;
@@ -483,7 +498,7 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
             if (before == kConsumerWarps - 1) {
                 sm.rel[s] = 0u;
                 int rt2, st2;
-                if (tile_of(p, n_units, it + kStages, rt2, st2)) {
+                if (tile_of(p, n_units, it + Sm::kNS, rt2, st2)) {
                     stage_meta(sm, p, s, rt2);
                     // bytes expected before the arrival, so the phase waits for them;
                     // the arrival releases the metadata
@@ -501,7 +516,7 @@ __device__ __forceinline__ int consumer_loop(DrSmem &sm, const CUtensorMap *tm_r
 }
 
 template <bool kSR>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, DrCfg<kSR>::kCtasPerSm)
 direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
                       const __grid_constant__ CUtensorMap tm_scales,
                       const __grid_constant__ CUtensorMap tm_trailer,
@@ -509,11 +524,12 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
                       const __grid_constant__ DrArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
-    DrSmem &sm = *reinterpret_cast<DrSmem *>(
+    using Sm = typename DrCfg<kSR>::Smem;
+    Sm &sm = *reinterpret_cast<Sm *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < Sm::kNS; ++i) {
             mbar_init(&sm.full[i], 1);
             sm.rel[i] = 0u;
             for (int q = 0; q < kConsumerWarps / 2; ++q)
@@ -551,7 +567,6 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
         const float se = p.scale_enc[i];
         sm.se_cache[i] = se;
-        sm.ce_cache[i] = __fdiv_rn(se, 6.0f);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -573,7 +588,7 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     // warps may have stopped at different tiles)
     if (threadIdx.x == 0) {
         for (int i = sm.consumed; i < sm.issued; ++i)
-            (void)mbar_wait_bounded(&sm.full[i % kStages], (uint32_t)(i / kStages) & 1u);
+            (void)mbar_wait_bounded(&sm.full[i % Sm::kNS], (uint32_t)(i / Sm::kNS) & 1u);
     }
 }
 
@@ -660,14 +675,15 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
         a.rcp[code] = (v == 0.0f || code == 127) ? 0.0f : 1.0f / v;   // IEEE single division: RN(1/v)
     }
 
-    const size_t smem = sizeof(DrSmem) + 1024;
+    const bool sr = rounding == 1;
+    const size_t smem = (sr ? sizeof(DrCfg<true>::Smem) : sizeof(DrCfg<false>::Smem)) + 1024;
     static int done_rn[2] = {0, 0}, done_sr[2] = {0, 0};
-    err = rounding == 1 ? ensure_smem_limit(direct_receive_kernel<true>, c.device, (int)smem, done_sr)
-                                    : ensure_smem_limit(direct_receive_kernel<false>, c.device, (int)smem, done_rn);
+    err = sr ? ensure_smem_limit(direct_receive_kernel<true>, c.device, (int)smem, done_sr)
+             : ensure_smem_limit(direct_receive_kernel<false>, c.device, (int)smem, done_rn);
     if (err != cudaSuccess)
         return err;
     const int64_t max_units = (int64_t)(R_cap / kTileRows) * a.n_strips;
-    int64_t grid = 2 * (int64_t)c.num_sms;
+    int64_t grid = (int64_t)(sr ? DrCfg<true>::kCtasPerSm : DrCfg<false>::kCtasPerSm) * c.num_sms;
     if (grid > max_units)
         grid = max_units;
     if (grid < 1)
