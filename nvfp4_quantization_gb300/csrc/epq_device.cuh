@@ -96,6 +96,14 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code)
     return f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(code & 0xffu)).x;
 }
 
+// Two FP32 -> packed f16x2, round to nearest even; `lo` in the low half.
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Two FP32 -> packed bf16x2, round to nearest even; `lo` in the low half.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi)
 {
@@ -278,6 +286,28 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
                  "selp.u32 %0, 1, 0, po;\n\t}"
                  : "=r"(out) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
     return out != 0;
+}
+
+// RN(a * b + c) with a, b the halves H_A, H_B (0 = low, 1 = high) of two
+// packed f16 pairs and c, the result FP32: one mixed-precision FMA (the
+// product of two f16 values is exact in FP32, so this rounds once).
+template <int HA, int HB>
+__device__ __forceinline__ float fma_f16h(uint32_t a, uint32_t b, float c)
+{
+    float d;
+    if (HA == 0 && HB == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    else if (HA == 1 && HB == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a1, b0, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    else if (HA == 0 && HB == 1)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a0, b1, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    else
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    return d;
 }
 
 // max(m, |a|, |b|) in one three-input maximum (finite inputs).

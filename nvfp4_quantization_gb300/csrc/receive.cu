@@ -58,6 +58,7 @@ constexpr int kThreads = kConsumers;         // no producer warp: the last warp 
 constexpr uint32_t kStageTx = kTileRows * (kCodeBytes + kScaleBytes + 16);
 constexpr int kWarpRows = kTileRows / 2;     // rows of a tile one consumer warp handles
 constexpr int kWTabStride = kWarpRows + 2;   // float2 entries; pad: a warp's 4 column blocks hit distinct banks
+constexpr int kT16Stride = kWarpRows + 4;    // f16 entries of the f16 table (same storage); distinct banks too
 constexpr int kMaxExperts = 1024;
 
 struct StageMeta {
@@ -257,25 +258,43 @@ __device__ __forceinline__ void st32g(void *p, uint4 a, uint4 b)
 // One 16-row block of the thread's two columns: decode, RHT, block scales,
 // E2M1 codes.  Returns the 8 code bytes of each column (cw0, cw1) and the two
 // E4M3 scale codes (s2: column 0 in the low byte).
-template <bool kSR, bool kFastR, class Sm>
-__device__ __forceinline__ void rht_block(const Sm &sm, int s, const float2 *tab, const float *rtab, int c,
-                                          int r0, float ce, const DrArgs &p, const StageMeta &m, int h0, int rl,
-                                          uint2 &cw0, uint2 &cw1, uint32_t &s2)
+template <bool kSR, bool kFastR, bool kF16, class Sm>
+__device__ __forceinline__ void rht_block(const Sm &sm, int s, const void *tab, const float *rtab, int c,
+                                          int r0, float ce, float se, const DrArgs &p, const StageMeta &m, int h0,
+                                          int rl, uint2 &cw0, uint2 &cw1, uint32_t &s2)
 {
-    // tab: this column block's decode scales of rows r0 .. r0+15, as (sc, sc)
-    const float4 *tp = reinterpret_cast<const float4 *>(tab);
     float2 u[16];
+    if (kF16) {
+        // tab: the column block's decode scales of rows r0 .. r0+15 as f16,
+        // rows (i, i+1) in one word, scaled by the warp tile's 2^-K; each
+        // decoded value q w is an exact f16 x f16 product, made and summed by
+        // one mixed-precision FMA (the same single rounding as below)
+        const uint32_t *tp = reinterpret_cast<const uint32_t *>(tab);
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-        const float4 t4 = tp[i >> 1];
-        const float2 qa = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i][c]));
-        const float2 qb = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i + 1][c]));
-        // len = 1 butterflies on the decoded values, which are exact products:
-        // one rounding each, fl(da + qb tb) and fl(da - qb tb), as a fused
-        // multiply-add with the exact product qb tb gives
-        const float2 da = mul2(qa, make_float2(t4.x, t4.y));
-        u[i] = __ffma2_rn(qb, make_float2(t4.z, t4.w), da);
-        u[i + 1] = __ffma2_rn(qb, make_float2(-t4.z, -t4.w), da);
+        for (int i = 0; i < 16; i += 2) {
+            const uint32_t w2 = tp[i >> 1];
+            const uint32_t qa = cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i][c]);
+            const uint32_t qb = cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i + 1][c]);
+            const uint32_t nqb = qb ^ 0x80008000u;
+            const float dax = fma_f16h<0, 0>(qa, w2, -0.0f), day = fma_f16h<1, 0>(qa, w2, -0.0f);
+            u[i] = make_float2(fma_f16h<0, 1>(qb, w2, dax), fma_f16h<1, 1>(qb, w2, day));
+            u[i + 1] = make_float2(fma_f16h<0, 1>(nqb, w2, dax), fma_f16h<1, 1>(nqb, w2, day));
+        }
+    } else {
+        // tab: this column block's decode scales of rows r0 .. r0+15, as (sc, sc)
+        const float4 *tp = reinterpret_cast<const float4 *>(tab);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const float4 t4 = tp[i >> 1];
+            const float2 qa = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i][c]));
+            const float2 qb = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i + 1][c]));
+            // len = 1 butterflies on the decoded values, which are exact products:
+            // one rounding each, fl(da + qb tb) and fl(da - qb tb), as a fused
+            // multiply-add with the exact product qb tb gives
+            const float2 da = mul2(qa, make_float2(t4.x, t4.y));
+            u[i] = __ffma2_rn(qb, make_float2(t4.z, t4.w), da);
+            u[i + 1] = __ffma2_rn(qb, make_float2(-t4.z, -t4.w), da);
+        }
     }
     // remaining Walsh-Hadamard butterflies, len = 2, 4, 8
 #pragma unroll
@@ -306,7 +325,7 @@ __device__ __forceinline__ void rht_block(const Sm &sm, int s, const float2 *tab
         // s = 0 gives y = 0 and r = 0
         const float2 y2 = make_float2(sm.rcp[s2 & 0xffu], sm.rcp[(s2 >> 8) & 0xffu]);
         const float2 sv = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(s2 & 0xffffu));
-        const float2 se2 = make_float2(m.se, m.se);
+        const float2 se2 = make_float2(se, se);
         const float2 q = mul2(se2, y2);
         const float2 e = __ffma2_rn(make_float2(-sv.x, -sv.y), q, se2);
         r2 = __ffma2_rn(e, y2, q);
@@ -384,27 +403,63 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
         }
 
         // this warp's decode scales: rows 64 hh + {lane, lane + 32}, column
-        // blocks 4 cq .. 4 cq + 3, with the RHT sign and the 1/4 folded in
+        // blocks 4 cq .. 4 cq + 3, with the RHT sign and the 1/4 folded in.
+        // When the token exponents k of the warp's rows with a nonzero scale
+        // lie within 13 of their maximum K, every s_b 2^(k - K - 2) is an
+        // exact f16 (no lower bit below 2^-24, at most 112): the block routine
+        // then runs on the values scaled by 2^-K (exact: powers of two), with
+        // S_enc and S_enc / 6 scaled by 2^K so that every rounding is the same.
+        uint32_t w4v[2], stv[2];
+        int kmax = -1000, kmin = 1000;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = 64 * hh + lane + 32 * h;
+            stv[h] = sm.trailer[s][r][0];
+            w4v[h] = *reinterpret_cast<const uint32_t *>(&sm.scales[s][r][4 * cq]);
+            const int k = (int)(stv[h] >> 23) - 127;
+            if (w4v[h] != 0u) {
+                kmax = max(kmax, k);
+                kmin = min(kmin, k);
+            }
+        }
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        const int K = kmax >= kmin ? kmax : 0;
+        const float se16 = m.se * exp2i(K), ce16 = m.ce * exp2i(K);
+        const bool f16 = kmin >= K - 13 && se16 >= 0x1p-100f && se16 <= 0x1p100f;
+        uint16_t(*t16)[kT16Stride] = reinterpret_cast<uint16_t(*)[kT16Stride]>(&tab[0][0]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int rloc = lane + 32 * h, r = 64 * hh + rloc;
-            float rs = u2f(sm.trailer[s][r][0]) * 0.25f;
-            if ((p.sign_mask >> (r & 15)) & 1u)
-                rs = -rs;
-            const uint32_t w4 = *reinterpret_cast<const uint32_t *>(&sm.scales[s][r][4 * cq]);
+            const bool neg = (p.sign_mask >> (r & 15)) & 1u;
+            const uint32_t w4 = w4v[h];
             const float2 a = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w4 & 0xffffu));
             const float2 b = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w4 >> 16));
-            const float v0 = a.x * rs, v1 = a.y * rs, v2 = b.x * rs, v3 = b.y * rs;
-            tab[0][rloc] = make_float2(v0, v0);
-            tab[1][rloc] = make_float2(v1, v1);
-            tab[2][rloc] = make_float2(v2, v2);
-            tab[3][rloc] = make_float2(v3, v3);
+            if (f16) {
+                const int k = (int)(stv[h] >> 23) - 127;
+                float f = w4 != 0u ? exp2i(k - K - 2) : 0.0f;
+                if (neg)
+                    f = -f;
+                const uint32_t lo = cvt_f16x2(a.x * f, a.y * f), hi = cvt_f16x2(b.x * f, b.y * f);
+                t16[0][rloc] = (uint16_t)lo;
+                t16[1][rloc] = (uint16_t)(lo >> 16);
+                t16[2][rloc] = (uint16_t)hi;
+                t16[3][rloc] = (uint16_t)(hi >> 16);
+            } else {
+                float rs = u2f(stv[h]) * 0.25f;
+                if (neg)
+                    rs = -rs;
+                const float v0 = a.x * rs, v1 = a.y * rs, v2 = b.x * rs, v3 = b.y * rs;
+                tab[0][rloc] = make_float2(v0, v0);
+                tab[1][rloc] = make_float2(v1, v1);
+                tab[2][rloc] = make_float2(v2, v2);
+                tab[3][rloc] = make_float2(v3, v3);
+            }
         }
         const float *rtab = sm.wrtab[warp];
-        // S_enc / s by a Markstein step when S_enc is in range, else from this
-        // warp's table of the expert's 128 quotients
-        const bool fast_r = m.se >= 0x1p-100f && m.se <= 0x1p100f;
-        if (!fast_r && m.e != cur_e) {
+        // S_enc / s by a Markstein step on the f16 path; else from this warp's
+        // table of the expert's 128 quotients
+        if (!f16 && m.e != cur_e) {
             cur_e = m.e;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -419,6 +474,7 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
         uint32_t csc0 = 0u, csc1 = 0u;
         if (h0 < H) {
             const float2 *ctab = &tab[lane >> 3][0];
+            const uint32_t *c16 = reinterpret_cast<const uint32_t *>(&t16[lane >> 3][0]);
             uint8_t *d0 = p.cw_codes + (int64_t)m.off * (H / 2) + (int64_t)h0 * (m.n / 2) + (rl + 64 * hh) / 2;
             uint8_t *d1 = d0 + (m.n / 2);
             uint32_t sc0 = 0u, sc1 = 0u;
@@ -428,14 +484,16 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
                 uint2 a0, a1, b0, b1;
                 uint32_t s2a, s2b;
                 const int r0 = 64 * hh + 32 * bp;
-                if (fast_r) {
-                    rht_block<kSR, true>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, p, m, h0, rl, a0, a1, s2a);
-                    rht_block<kSR, true>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, p, m, h0, rl, b0, b1,
-                                         s2b);
+                if (f16) {
+                    rht_block<kSR, true, true>(sm, s, c16 + 16 * bp, rtab, pc, r0, ce16, se16, p, m, h0, rl, a0, a1,
+                                               s2a);
+                    rht_block<kSR, true, true>(sm, s, c16 + 16 * bp + 8, rtab, pc, r0 + 16, ce16, se16, p, m, h0, rl,
+                                               b0, b1, s2b);
                 } else {
-                    rht_block<kSR, false>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, p, m, h0, rl, a0, a1, s2a);
-                    rht_block<kSR, false>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, p, m, h0, rl, b0, b1,
-                                          s2b);
+                    rht_block<kSR, false, false>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, m.se, p, m, h0, rl, a0,
+                                                 a1, s2a);
+                    rht_block<kSR, false, false>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, m.se, p, m, h0,
+                                                 rl, b0, b1, s2b);
                 }
                 q0[bp] = make_uint4(a0.x, a0.y, b0.x, b0.y);
                 q1[bp] = make_uint4(a1.x, a1.y, b1.x, b1.y);
