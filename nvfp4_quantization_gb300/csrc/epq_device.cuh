@@ -310,6 +310,24 @@ __device__ __forceinline__ float fma_f16h(uint32_t a, uint32_t b, float c)
     return d;
 }
 
+// Thread-block cluster: barrier over all threads of all CTAs of the cluster,
+// with release / acquire ordering of the shared-memory writes before it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// A 32-bit word at the same shared-memory offset as `p`, in the CTA of the
+// cluster with rank `rank`.
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const void *p, uint32_t rank)
+{
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote)
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // max(m, |a|, |b|) in one three-input maximum (finite inputs).
 __device__ __forceinline__ float max3_abs(float m, float a, float b)
 {

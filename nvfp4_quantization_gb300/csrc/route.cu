@@ -19,8 +19,16 @@
 //     all in token order.
 // The barrier waits are bounded: on timeout EP_DEV_ERR_TIMEOUT is raised and
 // the outputs are invalid.
+// Batches of at most 16 chunks (8192 tokens) with k <= 8 run as one
+// thread-block cluster instead, when the device can place it: the totals stay
+// in shared memory, the hardware cluster barrier replaces the grid barrier and
+// phase 2 reads the other CTAs' totals through distributed shared memory.
 #include "epq_device.cuh"
 #include "epq_internal.h"
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 namespace epq {
 
@@ -117,7 +125,13 @@ __device__ bool grid_barrier(uint32_t *count, uint32_t *gen, uint32_t g, uint32_
 // Fast path: one 512-token chunk per CTA and k <= 8: the validated ids and
 // the ranks of a thread's slots stay in registers between the phases.
 constexpr int kRegSlots = 8;
+constexpr int kMaxClusterCtas = 16;   // largest (non-portable) thread-block cluster
 
+// kCluster: the whole grid is one thread-block cluster (at most 16 CTAs):
+// the per-CTA totals stay in shared memory, the grid barrier is the cluster
+// barrier and phase 2 reads the other CTAs' totals through distributed shared
+// memory, so no global round trip separates the phases.
+template <bool kCluster>
 __global__ void __launch_bounds__(kChunk)
 route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A,
                       int32_t *__restrict__ offsets, int32_t *__restrict__ counts, int32_t *__restrict__ dest,
@@ -129,6 +143,7 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
     int *tot = reinterpret_cast<int *>(pre + (size_t)E * kWords);  // [E]
     int *base = tot + E;                         // [E]
     int *off = base + E;                         // [E]
+    int *myhist = off + E;                       // [E] this CTA's totals (cluster variant)
     __shared__ int wtmp[32];
     __shared__ int flag;
 
@@ -138,7 +153,7 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x, nctas = gridDim.x;
     int32_t *hist = reinterpret_cast<int32_t *>(ws + kWsHeader);   // [nctas][E]
-    const uint32_t g0 = tid == 0 ? ld_relaxed_gpu(ws + 1) : 0u;  // barrier generation before arrival
+    const uint32_t g0 = (!kCluster && tid == 0) ? ld_relaxed_gpu(ws + 1) : 0u;  // barrier generation before arrival
     const int64_t t = (int64_t)cta * kChunk + tid;
 
     int raw[kRegSlots], ev[kRegSlots], rk[kRegSlots];
@@ -187,8 +202,12 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
         }
         if (lane < kWords)
             pre[e * kWords + lane] = x - c;
-        if (lane == kWords - 1)
-            hist[(int64_t)cta * E + e] = (int)x;
+        if (lane == kWords - 1) {
+            if (kCluster)
+                myhist[e] = (int)x;
+            else
+                hist[(int64_t)cta * E + e] = (int)x;
+        }
     }
     __syncthreads();
 #pragma unroll
@@ -197,23 +216,39 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
         rk[j] = e >= 0 ? (int)(pre[e * kWords + warp] + __popc(mask[e * kWords + warp] & ((1u << lane) - 1u))) : 0;
     }
 
-    if (!grid_barrier(ws, ws + 1, g0, (uint32_t)nctas, &flag)) {
-        if (tid == 0)
-            raise_status(status, kDevErrTimeout);
-        return;
-    }
-
-    for (int e = tid; e < E; e += kChunk) {
-        int p = 0, all = 0;
+    if (kCluster) {
+        cluster_sync();   // every CTA's totals written
+        for (int e = tid; e < E; e += kChunk) {
+            int p = 0, all = 0;
 #pragma unroll 8
-        for (int c = 0; c < nctas; ++c) {
-            const int h = __ldcg(hist + (int64_t)c * E + e);
-            p += (c < cta) ? h : 0;
-            all += h;
+            for (int c = 0; c < nctas; ++c) {
+                const int h = (int)ld_dsmem_u32(myhist + e, (uint32_t)c);
+                p += (c < cta) ? h : 0;
+                all += h;
+            }
+            base[e] = p;
+            tot[e] = all;
+            off[e] = (all + A - 1) / A * A;
         }
-        base[e] = p;
-        tot[e] = all;
-        off[e] = (all + A - 1) / A * A;
+        cluster_sync();   // every CTA done reading the others' totals
+    } else {
+        if (!grid_barrier(ws, ws + 1, g0, (uint32_t)nctas, &flag)) {
+            if (tid == 0)
+                raise_status(status, kDevErrTimeout);
+            return;
+        }
+        for (int e = tid; e < E; e += kChunk) {
+            int p = 0, all = 0;
+#pragma unroll 8
+            for (int c = 0; c < nctas; ++c) {
+                const int h = __ldcg(hist + (int64_t)c * E + e);
+                p += (c < cta) ? h : 0;
+                all += h;
+            }
+            base[e] = p;
+            tot[e] = all;
+            off[e] = (all + A - 1) / A * A;
+        }
     }
     __syncthreads();
     const int total = block_exclusive_scan(off, E, wtmp);
@@ -381,11 +416,13 @@ cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, in
                               int32_t *offsets, int32_t *counts, int32_t *dest, int32_t *hist,
                               uint32_t *status)
 {
-    const size_t smem = (size_t)E * kWords * 4u * 2u + (size_t)E * 4u * 3u;
-    static int done[2] = {0, 0}, done_reg[2] = {0, 0};
-    cudaError_t err = ensure_smem_limit(route_plan_kernel, c.device, 1024 * kWords * 8 + 1024 * 12, done);
+    const size_t smem = (size_t)E * kWords * 4u * 2u + (size_t)E * 4u * 4u;
+    static int done[2] = {0, 0}, done_reg[2] = {0, 0}, done_cl[2] = {0, 0};
+    cudaError_t err = ensure_smem_limit(route_plan_kernel, c.device, 1024 * kWords * 8 + 1024 * 16, done);
     if (err == cudaSuccess)
-        err = ensure_smem_limit(route_plan_reg_kernel, c.device, 1024 * kWords * 8 + 1024 * 12, done_reg);
+        err = ensure_smem_limit(route_plan_reg_kernel<false>, c.device, 1024 * kWords * 8 + 1024 * 16, done_reg);
+    if (err == cudaSuccess)
+        err = ensure_smem_limit(route_plan_reg_kernel<true>, c.device, 1024 * kWords * 8 + 1024 * 16, done_cl);
     if (err != cudaSuccess)
         return err;
     int per_sm = 0;
@@ -412,8 +449,45 @@ cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, in
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cpc == 1 && k <= kRegSlots && nctas <= kMaxClusterCtas) {
+        // one cluster of all CTAs, if the device can place it
+        // (placement answer cached per device, cluster size and shared-memory size class)
+        static std::mutex mu;
+        static std::map<std::tuple<int, int, size_t>, bool> fits;
+        cudaLaunchAttribute cl[1];
+        cl[0].id = cudaLaunchAttributeClusterDimension;
+        cl[0].val.clusterDim.x = (unsigned)nctas;
+        cl[0].val.clusterDim.y = 1;
+        cl[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t ccfg = cfg;
+        ccfg.attrs = cl;
+        ccfg.numAttrs = 1;
+        bool ok;
+        {
+            std::lock_guard<std::mutex> g(mu);
+            const auto key = std::make_tuple(c.device, nctas, smem);
+            auto it = fits.find(key);
+            if (it == fits.end()) {
+                if (nctas > 8 &&
+                    cudaFuncSetAttribute(route_plan_reg_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                         1) != cudaSuccess)
+                    (void)cudaGetLastError();
+                int nclusters = 0;
+                ok = cudaOccupancyMaxActiveClusters(&nclusters, route_plan_reg_kernel<true>, &ccfg) == cudaSuccess &&
+                     nclusters >= 1;
+                if (!ok)
+                    (void)cudaGetLastError();
+                fits.emplace(key, ok);
+            } else {
+                ok = it->second;
+            }
+        }
+        if (ok)
+            return cudaLaunchKernelEx(&ccfg, route_plan_reg_kernel<true>, topk, T, k, E, A, offsets, counts, dest,
+                                      reinterpret_cast<uint32_t *>(hist), status);
+    }
     if (cpc == 1 && k <= kRegSlots)
-        return cudaLaunchKernelEx(&cfg, route_plan_reg_kernel, topk, T, k, E, A, offsets, counts, dest,
+        return cudaLaunchKernelEx(&cfg, route_plan_reg_kernel<false>, topk, T, k, E, A, offsets, counts, dest,
                                   reinterpret_cast<uint32_t *>(hist), status);
     return cudaLaunchKernelEx(&cfg, route_plan_kernel, topk, T, k, E, A, cpc, offsets, counts, dest,
                               reinterpret_cast<uint32_t *>(hist), status);
