@@ -186,8 +186,9 @@ class BufferSet:
 
     def route_pack(self):
         w, nq = self.w, self.nq
-        nq.ep_route_plan(self.topk, w.E, w.A, R_cap=self.plan.R_cap, plan=self.plan, workspace=self.ws)
-        nq.ep_nvfp4_pack(self.tok, self.plan, rows=self.rows, rounding=w.rounding, seed=w.seed)
+        # route plan + pack in one call: the pack encodes its first tokens while the routing kernel runs
+        nq.ep_nvfp4_dispatch(self.tok, self.topk, w.E, w.A, plan=self.plan, workspace=self.ws, rows=self.rows,
+                             rounding=w.rounding, seed=w.seed)
 
     def receive(self):
         w, nq = self.w, self.nq
@@ -502,7 +503,7 @@ def main():
                      "traffic": profiled_traffic("direct_receive", DR_SOURCES)},
         "e2e": {"value": world * r["T"] / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"],
-                "api": "eager ep_route_plan / ep_nvfp4_pack / ep_nvfp4_direct_receive on two streams, "
+                "api": "eager ep_nvfp4_dispatch / ep_nvfp4_direct_receive on two streams, "
                        "alternate steps (double buffering)", "checked": e2e["ok"]},
         "other_calls": {name: {"ms": v["ms"], "gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9,
                                "frac": v["bytes"] / (v["ms"] * 1e-3) / 1e9 / peak, "bytes": v["bytes"],

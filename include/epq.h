@@ -181,6 +181,29 @@ ep_status ep_nvfp4_pack(const void *tokens_bf16, int64_t T, int64_t H,
                         uint32_t *dev_status, void *stream);
 
 /*
+ * ep_nvfp4_dispatch -- ep_route_plan followed by ep_nvfp4_pack, in one call.
+ * TE PR #3753, PR description: the NVFP4 dispatch routes each token and sends
+ * it as one packed NVFP4 row; here the routing plan and the pack run back to
+ * back on `stream`.
+ *   Arguments: those of ep_route_plan (topk_idx, T, k, E, A, R_cap,
+ *   expert_offsets, expert_counts, dest, workspace, ws_bytes) and of
+ *   ep_nvfp4_pack (tokens_bf16, H, rows, rounding, seed); every check of both
+ *   calls is made before anything is enqueued.  Outputs, device status and
+ *   errors: exactly those of the two calls made in that order.
+ *   Timing: the routing kernel starts only after all earlier work on `stream`
+ *   has finished, so the pack kernel reads and encodes its first tokens while
+ *   the routing kernel still runs and waits for it only before reading `dest`
+ *   (the separate ep_nvfp4_pack reads no token before that wait).
+ */
+ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16,
+                            int64_t T, int64_t H, int k, int E, int A,
+                            int64_t R_cap, int32_t *expert_offsets,
+                            int32_t *expert_counts, int32_t *dest,
+                            void *workspace, size_t ws_bytes, uint8_t *rows,
+                            int rounding, uint64_t seed, uint32_t *dev_status,
+                            void *stream);
+
+/*
  * ep_nvfp4_unpack -- decode packed rows to BF16 (the path used when direct
  * receive is off).  TE PR #3753, PR description: "Otherwise the rows are
  * decoded to BF16"; commit "grad direct-receive opt-out": the opt-out returns

@@ -27,7 +27,7 @@ EP_ROUTE_STATIC_SCRATCH_BYTES = 262144   # mirrors the macro in include/epq.h
 
 # every symbol include/epq.h declares
 SYMBOLS = ("ep_nvfp4_row_bytes", "ep_rows_capacity", "ep_route_workspace_bytes", "ep_route_plan",
-           "ep_route_plan_noalloc", "ep_nvfp4_pack", "ep_nvfp4_unpack", "ep_nvfp4_direct_receive",
+           "ep_route_plan_noalloc", "ep_nvfp4_pack", "ep_nvfp4_dispatch", "ep_nvfp4_unpack", "ep_nvfp4_direct_receive",
            "ep_mxfp8_pack", "ep_status_string")
 
 
@@ -57,6 +57,9 @@ def _declare(L):
     L.ep_route_plan_noalloc.restype = _I32
     L.ep_nvfp4_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _I32, _U64, _P, _P]
     L.ep_nvfp4_pack.restype = _I32
+    L.ep_nvfp4_dispatch.argtypes = [_P, _P, _I64, _I64, _I32, _I32, _I32, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                                    _I32, _U64, _P, _P]
+    L.ep_nvfp4_dispatch.restype = _I32
     L.ep_nvfp4_unpack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _P]
     L.ep_nvfp4_unpack.restype = _I32
     L.ep_nvfp4_direct_receive.argtypes = [_P, _I64, _I64, _P, _I32, ctypes.POINTER(EpGrouped), _I32, _U64,

@@ -122,6 +122,42 @@ def ep_nvfp4_pack(tokens: torch.Tensor, plan: RoutePlan, rows: torch.Tensor | No
     return rows
 
 
+def ep_nvfp4_dispatch(tokens: torch.Tensor, topk_idx: torch.Tensor, E: int, A: int = DEFAULT_ALIGNMENT,
+                      R_cap: int | None = None, plan: RoutePlan | None = None,
+                      workspace: torch.Tensor | None = None, rows: torch.Tensor | None = None,
+                      rounding: int = EP_ROUND_RNE, seed: int = 0, status: torch.Tensor | None = None,
+                      stream=None) -> tuple[RoutePlan, torch.Tensor]:
+    """ep_route_plan then ep_nvfp4_pack in one C call (the pack overlaps the
+    routing kernel); returns (plan, rows)."""
+    _need_cuda(tokens, "tokens", torch.bfloat16)
+    _need_cuda(topk_idx, "topk_idx", torch.int32)
+    T, k = topk_idx.shape
+    if tokens.shape[0] != T:
+        raise ValueError("tokens and topk_idx disagree on T")
+    H = tokens.shape[1]
+    dev = topk_idx.device
+    if R_cap is None:
+        R_cap = plan.R_cap if plan is not None else rows_capacity(T, k, E, A)
+    if plan is None:
+        plan = RoutePlan(torch.empty(E + 1, dtype=torch.int32, device=dev),
+                         torch.empty(E, dtype=torch.int32, device=dev),
+                         torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+                         T, k, E, A, R_cap, status if status is not None else new_status(dev))
+    if workspace is None:
+        workspace = new_route_workspace(T, k, E, dev)
+    if rows is None:
+        rows = torch.empty((R_cap, row_bytes(H)), dtype=torch.uint8, device=dev)
+    _need_cuda(rows, "rows", torch.uint8)
+    if rows.shape[0] < R_cap:
+        raise ValueError("rows has fewer than R_cap rows")
+    st = _lib.lib().ep_nvfp4_dispatch(_ptr(topk_idx), _ptr(tokens), T, H, k, E, A, R_cap, _ptr(plan.offsets),
+                                      _ptr(plan.counts), _ptr(plan.dest), _ptr(workspace), workspace.numel() * 4,
+                                      _ptr(rows), int(rounding), int(seed) & ((1 << 64) - 1), _ptr(plan.status),
+                                      _stream(stream))
+    check("ep_nvfp4_dispatch", st)
+    return plan, rows
+
+
 def ep_nvfp4_unpack(rows: torch.Tensor, H: int, offsets: torch.Tensor, E: int,
                     out: torch.Tensor | None = None, status: torch.Tensor | None = None,
                     stream=None) -> torch.Tensor:

@@ -177,6 +177,41 @@ ep_status ep_nvfp4_pack(const void *tokens_bf16, int64_t T, int64_t H, const int
                                               seed, dev_status));
 }
 
+ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16, int64_t T, int64_t H, int k, int E,
+                            int A, int64_t R_cap, int32_t *expert_offsets, int32_t *expert_counts, int32_t *dest,
+                            void *workspace, size_t ws_bytes, uint8_t *rows, int rounding, uint64_t seed,
+                            uint32_t *dev_status, void *stream)
+{
+    if (!expert_offsets || !expert_counts || !workspace || !dev_status || !rows ||
+        (T > 0 && (!topk_idx || !dest || !tokens_bf16)))
+        return EP_ERR_NULL;
+    if (T < 0 || T * (int64_t)k > (int64_t)INT32_MAX || k < 1 || k > 32 || E < 1 || E > 1024 ||
+        !shape_ok(T, H, k, E))
+        return EP_ERR_SHAPE;
+    if (A <= 0 || A % 128 != 0 || !aligned16(tokens_bf16) || !aligned16(rows))
+        return EP_ERR_ALIGN;
+    if (R_cap < ep_rows_capacity(T, k, E, A) || R_cap > (int64_t)INT32_MAX)
+        return EP_ERR_CAPACITY;
+    if (ws_bytes < ep_route_workspace_bytes(T, k, E))
+        return EP_ERR_CAPACITY;
+    if (rounding != EP_ROUND_RNE && rounding != EP_ROUND_SR)
+        return EP_ERR_ARG;
+    const int dev = device_of(expert_offsets);
+    if (dev < 0 || !on_device(topk_idx, dev) || !on_device(tokens_bf16, dev) || !on_device(expert_counts, dev) ||
+        !on_device(dest, dev) || !on_device(workspace, dev) || !on_device(rows, dev) || !on_device(dev_status, dev))
+        return EP_ERR_DEVICE;
+    DeviceGuard g(dev);
+    if (!g.ok)
+        return EP_ERR_DEVICE;
+    LaunchCtx c{(cudaStream_t)stream, dev, sm_count(dev)};
+    cudaError_t err = epq::launch_route_plan(c, topk_idx, (int)T, k, E, A, expert_offsets, expert_counts, dest,
+                                             (int32_t *)workspace, dev_status);
+    if (err == cudaSuccess)
+        err = epq::launch_nvfp4_pack(c, (const uint16_t *)tokens_bf16, (int)T, (int)H, dest, k, expert_offsets,
+                                     expert_counts, E, rows, (int)R_cap, rounding, seed, dev_status, true);
+    return cuda_status(err);
+}
+
 ep_status ep_mxfp8_pack(const void *tokens_bf16, int64_t T, int64_t H, const int32_t *dest, int k,
                         const int32_t *expert_offsets, const int32_t *expert_counts, int E, uint8_t *buf,
                         int64_t R_cap, uint32_t *dev_status, void *stream)

@@ -52,14 +52,18 @@ cudaError_t ensure_smem_limit(K kernel, int device, int bytes, int *done_mask_wo
 }
 
 size_t route_workspace_bytes(int64_t T, int E);
+// Launched without programmatic dependency: it starts only once every earlier
+// kernel on the stream has finished (launch_nvfp4_pack's `early` relies on it).
 cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, int k, int E, int A,
                               int32_t *offsets, int32_t *counts, int32_t *dest, int32_t *hist,
                               uint32_t *status);
 
+// early: the launch directly follows launch_route_plan on the same stream,
+// so the tokens may be read before the wait for the routing kernel.
 cudaError_t launch_nvfp4_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                               const int32_t *dest, int k, const int32_t *offsets,
                               const int32_t *counts, int E, uint8_t *rows, int R_cap,
-                              int rounding, uint64_t seed, uint32_t *status);
+                              int rounding, uint64_t seed, uint32_t *status, bool early = false);
 
 cudaError_t launch_mxfp8_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                               const int32_t *dest, int k, const int32_t *offsets,

@@ -406,6 +406,14 @@ __device__ __forceinline__ void encode_lane_blocks(const uint32_t (&w)[NB][8], c
 // buffer, reduces the token amax with a warp reduction, encodes its blocks
 // and stores them to every destination row.  CTAs past the token CTAs write
 // the padding rows.
+//
+// `early` (set only when the routing kernel just before this one on the
+// stream was launched without programmatic dependency, so every earlier
+// kernel, and with it whatever wrote the tokens, finished before it began):
+// the tokens are complete when this grid starts, so each warp copies and
+// encodes its first token while the routing kernel still runs, and waits for
+// it only before reading the destinations.  Otherwise nothing is read before
+// the wait but an L2 prefetch of the first tokens (it returns no data).
 constexpr int kPackWarps = 4;
 // One buffer per warp: the next token's copy is issued as soon as the current
 // one is in registers, so it overlaps the encode and the stores; a second
@@ -419,27 +427,29 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
                        int k, const int32_t *__restrict__ offsets, const int32_t *__restrict__ counts, int E,
                        uint8_t *__restrict__ rows, int64_t S, int R_cap, const __grid_constant__ PhiloxKey key,
                        uint32_t *__restrict__ status, int n_tok_ctas, int pad_ctas,
-                       const __grid_constant__ RcpTable rcp)
+                       const __grid_constant__ RcpTable rcp, int early)
 {
     extern __shared__ __align__(128) uint8_t pbuf[];   // [kPackWarps][kBuf][2H]
     __shared__ float srcp[128];
     __shared__ uint64_t bar[kPackWarps][kBuf];
     pdl_launch_dependents();
+    if ((int)blockIdx.x >= n_tok_ctas) {
+        pdl_wait();
+        fill_padding(0, blockIdx.x - n_tok_ctas, pad_ctas, offsets, counts, E, R_cap, rows, S, H, status);
+        return;
+    }
     // Before the wait for the routing plan: pull this warp's first tokens
-    // into L2 (a prefetch returns no data, so it cannot observe a stale value)
-    if ((int)blockIdx.x < n_tok_ctas && (threadIdx.x & 31) == 0) {
+    // into L2 (the ones the first bulk copies do not fetch at once)
+    if ((threadIdx.x & 31) == 0) {
         const int tw = blockIdx.x * kPackWarps + (threadIdx.x >> 5);
-        for (int q = 0; q < kBuf + 1; ++q) {
+        for (int q = early ? kBuf : 0; q < kBuf + 1; ++q) {
             const int t = tw + q * n_tok_ctas * kPackWarps;
             if (t < T)
                 bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(tokens) + (int64_t)t * 2 * H, 2u * (uint32_t)H);
         }
     }
-    pdl_wait();
-    if ((int)blockIdx.x >= n_tok_ctas) {
-        fill_padding(0, blockIdx.x - n_tok_ctas, pad_ctas, offsets, counts, E, R_cap, rows, S, H, status);
-        return;
-    }
+    if (!early)
+        pdl_wait();
     for (int i = threadIdx.x; i < 128; i += blockDim.x)
         srcp[i] = rcp.v[i];
     if (threadIdx.x == 0) {
@@ -487,7 +497,8 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
             w[q][0] = v0.x; w[q][1] = v0.y; w[q][2] = v0.z; w[q][3] = v0.w;
             w[q][4] = v1.x; w[q][5] = v1.y; w[q][6] = v1.z; w[q][7] = v1.w;
         }
-        const int dl = lane < k ? __ldg(dest + (int64_t)t * k + lane) : -1;
+        // (the first token's destinations, under `early`, only after the wait)
+        int dl = (lane < k && (i > 0 || !early)) ? __ldg(dest + (int64_t)t * k + lane) : -1;
         uint32_t bm[NB];
         uint32_t amax = 0;
 #pragma unroll
@@ -514,6 +525,11 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
             encode_lane_blocks<NB, true, kSR>(w, bm, St, exp2i(-kt), srcp, key, (uint64_t)t, H, lane, code, sbyte);
         else
             encode_lane_blocks<NB, false, kSR>(w, bm, St, 0.0f, srcp, key, (uint64_t)t, H, lane, code, sbyte);
+        if (i == 0 && early) {
+            pdl_wait();
+            if (lane < k)
+                dl = __ldg(dest + (int64_t)t * k + lane);
+        }
         for (int j = 0; j < k; ++j) {
             const int d = __shfl_sync(0xffffffffu, dl, j);
             if (d < 0)
@@ -655,7 +671,7 @@ template <int NB>
 static cudaError_t launch_nvfp4_warp(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                                      const int32_t *dest, int k, const int32_t *offsets,
                                      const int32_t *counts, int E, uint8_t *rows, int R_cap,
-                                     int rounding, uint64_t seed, uint32_t *status)
+                                     int rounding, uint64_t seed, uint32_t *status, int early)
 {
     static const RcpTable rcp = make_rcp_table();
     const int pc = padding_ctas(c, E);
@@ -683,19 +699,19 @@ static cudaError_t launch_nvfp4_warp(const LaunchCtx &c, const uint16_t *tokens,
         tc = 1;
     if (rounding == 1)
         return launch_pdl(nvfp4_pack_warp_kernel<NB, true>, dim3(tc + pc), dim3(th), smem, c.stream, tokens, T, H,
-                          dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
+                          dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, early);
     return launch_pdl(nvfp4_pack_warp_kernel<NB, false>, dim3(tc + pc), dim3(th), smem, c.stream, tokens, T, H,
-                      dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
+                      dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, early);
 }
 
 cudaError_t launch_nvfp4_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                               const int32_t *dest, int k, const int32_t *offsets,
                               const int32_t *counts, int E, uint8_t *rows, int R_cap,
-                              int rounding, uint64_t seed, uint32_t *status)
+                              int rounding, uint64_t seed, uint32_t *status, bool early)
 {
     if (H % 512 == 0 && H <= 8192) {
         switch (H / 512) {
-#define EPQ_NB(n) case n: return launch_nvfp4_warp<n>(c, tokens, T, H, dest, k, offsets, counts, E, rows, R_cap, rounding, seed, status);
+#define EPQ_NB(n) case n: return launch_nvfp4_warp<n>(c, tokens, T, H, dest, k, offsets, counts, E, rows, R_cap, rounding, seed, status, early ? 1 : 0);
             EPQ_NB(1) EPQ_NB(2) EPQ_NB(3) EPQ_NB(4) EPQ_NB(5) EPQ_NB(6) EPQ_NB(7) EPQ_NB(8)
             EPQ_NB(9) EPQ_NB(10) EPQ_NB(11) EPQ_NB(12) EPQ_NB(13) EPQ_NB(14) EPQ_NB(15) EPQ_NB(16)
 #undef EPQ_NB

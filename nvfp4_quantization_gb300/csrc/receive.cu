@@ -23,8 +23,8 @@
 // Stages: a shared-memory ring of tiles (2 stages and 3 CTAs per SM for RNE,
 // 3 stages and 2 CTAs per SM for SR) loaded by 2-D TMA (codes 128 B
 // x 128 rows, scales 16 B x 128, row trailers 16 B x 128).  There is no
-// producer warp: thread 0 issues the first tiles' loads, and the last warp to
-// finish with a stage (an acquire-release counter) writes the metadata of the
+// producer warp: thread 0 issues the first tile's loads (the other stages'
+// once it has arrived), and the last warp to finish with a stage (an acquire-release counter) writes the metadata of the
 // tile kStages ahead (expert, its offsets, S_enc) and issues its loads.
 //
 // Warps (8): the rowwise operand leaves straight from the ring (TMA
@@ -227,17 +227,18 @@ expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *_
 }
 
 // Tile-kernel set-up (expert offsets in shared memory; thread 0): the loads of
-// the first min(kStages, tiles) tiles, before S_enc is known.
+// the first tile, before S_enc is known.  The other stages are loaded once the
+// first tile has arrived, so that at start-up, when every CTA asks at once,
+// each CTA's first tile is not queued behind the grid's second tiles.
 template <class Sm>
 __device__ __forceinline__ int tile_prologue(Sm &sm, const DrArgs &p, int n_units, const CUtensorMap *tmc,
                                              const CUtensorMap *tms, const CUtensorMap *tmt)
 {
-    int n = 0, rt, st;
-    while (n < Sm::kNS && tile_of(p, n_units, n, rt, st)) {
-        issue_tile(sm, tmc, tms, tmt, n, rt, st);
-        ++n;
-    }
-    return n;
+    int rt, st;
+    if (!tile_of(p, n_units, 0, rt, st))
+        return 0;
+    issue_tile(sm, tmc, tms, tmt, 0, rt, st);
+    return 1;
 }
 
 __device__ __forceinline__ void st16g(void *p, uint4 v)
@@ -636,6 +637,20 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
             mbar_arrive(&sm.full[it]);
         }
         sm.issued = pre;
+        // once the first tile is here, load the other stages (metadata, bytes
+        // expected, then the arrival that releases both); a wait that gives
+        // up is seen again, and handled, by the tile loop
+        if (pre == 1 && mbar_wait_bounded(&sm.full[0], 0u)) {
+            for (int n = 1; n < Sm::kNS; ++n) {
+                int rt, st;
+                if (!tile_of(p, n_units, n, rt, st))
+                    break;
+                stage_meta(sm, p, n, rt);
+                issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, n, rt, st);
+                mbar_arrive(&sm.full[n]);
+                sm.issued = n + 1;
+            }
+        }
     }
 
     const int done = consumer_loop<kSR>(sm, &tm_rw, &tm_rws, &tm_codes, &tm_scales, &tm_trailer, p, n_units);

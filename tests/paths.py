@@ -30,15 +30,19 @@ def assert_bytes_equal(got: np.ndarray, want: np.ndarray, what: str):
 class GpuRun:
     """The hot path on the GPU for one workload, with canary-filled outputs."""
 
-    def __init__(self, w, rowwise=True, mxfp8=False, unpack=False, R_cap=None):
+    def __init__(self, w, rowwise=True, mxfp8=False, unpack=False, R_cap=None, dispatch=False):
         self.w = w
         self.tok = to_dev_bf16(w.tokens)
         self.topk = torch.from_numpy(np.ascontiguousarray(w.topk)).cuda()
         self.R_cap = R_cap or nq.rows_capacity(w.T, w.k, w.E, w.A)
-        self.plan = nq.ep_route_plan(self.topk, w.E, w.A, R_cap=self.R_cap)
         S = nq.row_bytes(w.H)
         self.rows = torch.full((self.R_cap, S), CANARY, dtype=torch.uint8, device="cuda")
-        nq.ep_nvfp4_pack(self.tok, self.plan, rows=self.rows, rounding=w.rounding, seed=w.seed)
+        if dispatch:   # route plan + pack in one call
+            self.plan, _ = nq.ep_nvfp4_dispatch(self.tok, self.topk, w.E, w.A, R_cap=self.R_cap, rows=self.rows,
+                                                rounding=w.rounding, seed=w.seed)
+        else:
+            self.plan = nq.ep_route_plan(self.topk, w.E, w.A, R_cap=self.R_cap)
+            nq.ep_nvfp4_pack(self.tok, self.plan, rows=self.rows, rounding=w.rounding, seed=w.seed)
         g = nq.alloc_grouped(self.R_cap, w.H, w.E, "cuda", rowwise=rowwise)
         for t in g.values():
             t.view(torch.uint8).fill_(CANARY)

@@ -30,17 +30,19 @@ FLT_MAX = np.float32(3.4028234663852886e38)
 
 
 class FullRun:
-    """The benchmark's step on one full-size batch (route plan, pack, direct
-    receive; MXFP8 pack for the last batch), outputs kept on the device."""
+    """The benchmark's step on one full-size batch (route plan and pack in one
+    dispatch call, direct receive; MXFP8 pack for the last batch), outputs
+    kept on the device."""
 
     def __init__(self, cfg):
         w = workloads.make(cfg)
         self.w = w
         self.tok = to_dev_bf16(w.tokens)
         self.topk = torch.from_numpy(np.ascontiguousarray(w.topk)).cuda()
-        self.plan = nq.ep_route_plan(self.topk, w.E, w.A)
+        # the benchmark's calls: route plan + pack in one dispatch call
+        self.plan, self.rows = nq.ep_nvfp4_dispatch(self.tok, self.topk, w.E, w.A, rounding=w.rounding,
+                                                    seed=w.seed)
         self.R_cap = self.plan.R_cap
-        self.rows = nq.ep_nvfp4_pack(self.tok, self.plan, rounding=w.rounding, seed=w.seed)
         self.out = nq.ep_nvfp4_direct_receive(self.rows, w.H, self.plan.offsets, w.E, rounding=w.rounding,
                                               seed=w.seed, sign_mask=w.sign_mask, status=self.plan.status)
         self.mx = nq.ep_mxfp8_pack(self.tok, self.plan) if "mxfp8_pack" in w.ops else None

@@ -35,6 +35,27 @@ def test_parity_config(name):
     compare_runs(g, o)
 
 
+@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg4", "cfg5", "cfg4_ragged_H"])
+def test_parity_dispatch(name):
+    """ep_nvfp4_dispatch (route plan + pack in one call, the pack encoding
+    its first tokens while the routing kernel runs) against the oracle; the
+    ragged-H case takes the pack kernel without the early reads."""
+    c = CASES[name]
+    w = workloads.make(c["cfg"], **c["kw"])
+    g = GpuRun(w, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False), dispatch=True)
+    o = OracleRun(w, g.R_cap, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False))
+    compare_runs(g, o)
+
+
+def test_parity_dispatch_sr_many_tokens_per_warp():
+    """More tokens than the pack's resident warps (several tokens per warp
+    after the first), stochastic rounding, through ep_nvfp4_dispatch."""
+    w = workloads.make(4, T=9000, H=512, E=32, k=3)
+    g = GpuRun(w, dispatch=True)
+    o = OracleRun(w, g.R_cap)
+    compare_runs(g, o)
+
+
 def test_parity_rne_and_sr_on_same_tokens():
     base = workloads.make(4, T=200, H=512, E=16, k=4)
     for rounding, seed in ((0, 0), (1, 1), (1, 0xFFFFFFFFFFFF1234)):
@@ -189,6 +210,9 @@ def test_cuda_graph_capture_matches_eager():
         with torch.cuda.graph(graph, stream=s):
             nq.ep_route_plan(topk, w.E, w.A, R_cap=R_cap, plan=plan, workspace=ws)
             nq.ep_nvfp4_pack(tok, plan, rows=rows)
+            nq.ep_nvfp4_direct_receive(rows, w.H, plan.offsets, w.E, out=out, status=plan.status)
+            # the same again through the one-call dispatch (a second step in the graph)
+            nq.ep_nvfp4_dispatch(tok, topk, w.E, w.A, plan=plan, workspace=ws, rows=rows)
             nq.ep_nvfp4_direct_receive(rows, w.H, plan.offsets, w.E, out=out, status=plan.status)
     rows.fill_(CANARY)
     for t in out.values():
