@@ -23,8 +23,8 @@
 // Stages: a shared-memory ring of tiles (2 stages and 3 CTAs per SM for RNE,
 // 3 stages and 2 CTAs per SM for SR) loaded by 2-D TMA (codes 128 B
 // x 128 rows, scales 16 B x 128, row trailers 16 B x 128).  There is no
-// producer warp: thread 0 issues the first tile's loads (the other stages'
-// once it has arrived), and the last warp to finish with a stage (an acquire-release counter) writes the metadata of the
+// producer warp: thread 0 issues the first tile's loads as the CTA starts
+// (the other stages' once it has arrived), and the last warp to finish with a stage (an acquire-release counter) writes the metadata of the
 // tile kStages ahead (expert, its offsets, S_enc) and issues its loads.
 //
 // Warps (8): the rowwise operand leaves straight from the ring (TMA
@@ -224,21 +224,6 @@ expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *_
         }
         __syncthreads();
     }
-}
-
-// Tile-kernel set-up (expert offsets in shared memory; thread 0): the loads of
-// the first tile, before S_enc is known.  The other stages are loaded once the
-// first tile has arrived, so that at start-up, when every CTA asks at once,
-// each CTA's first tile is not queued behind the grid's second tiles.
-template <class Sm>
-__device__ __forceinline__ int tile_prologue(Sm &sm, const DrArgs &p, int n_units, const CUtensorMap *tmc,
-                                             const CUtensorMap *tms, const CUtensorMap *tmt)
-{
-    int rt, st;
-    if (!tile_of(p, n_units, 0, rt, st))
-        return 0;
-    issue_tile(sm, tmc, tms, tmt, 0, rt, st);
-    return 1;
 }
 
 __device__ __forceinline__ void st16g(void *p, uint4 v)
@@ -601,13 +586,22 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         tma_prefetch_desc(&tm_scales);
         tma_prefetch_desc(&tm_trailer);
     }
+    // The rows and the offsets were complete before this grid could start
+    // (expert_amax_kernel lets it launch only after its own wait on the pack
+    // has returned), so the first tile's loads go out before the wait on the
+    // amax kernel (only S_enc comes from it), and even before the expert
+    // offsets are read: tile 0 of this CTA is loaded if it lies inside the
+    // row capacity, and dropped unused if it lies past the rows in use.
+    // The other stages are loaded once it has arrived, so that at start-up,
+    // when every CTA asks at once, first tiles are not queued behind second
+    // ones.
+    const int rt0 = (int)blockIdx.x / p.n_strips, st0 = (int)blockIdx.x % p.n_strips;
+    const int pre = rt0 < p.R_cap / kTileRows ? 1 : 0;
+    if (threadIdx.x == 0 && pre)
+        issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, 0, rt0, st0);
     __syncthreads();
     pdl_launch_dependents();
 
-    // The rows and the offsets were complete before this grid could start
-    // (expert_amax_kernel lets it launch only after its own wait on the pack
-    // has returned), so the first tile loads go out before the wait on the
-    // amax kernel; only S_enc comes from it.
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x)
         sm.offs[i] = __ldg(p.offsets + i);
     for (int i = threadIdx.x; i < 128; i += blockDim.x)
@@ -620,8 +614,8 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         R = p.R_cap;
     }
     const int n_units = (R / kTileRows) * p.n_strips;
+    const bool use0 = (int)blockIdx.x < n_units;   // tile 0 holds rows in use
 
-    const int pre = threadIdx.x == 0 ? tile_prologue(sm, p, n_units, &tm_codes, &tm_scales, &tm_trailer) : 0;
     pdl_wait();
     for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
         const float se = p.scale_enc[i];
@@ -629,18 +623,18 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        // metadata of the preissued tiles; the arrivals release it
-        for (int it = 0; it < pre; ++it) {
-            int rt, st;
-            (void)tile_of(p, n_units, it, rt, st);
-            stage_meta(sm, p, it, rt);
-            mbar_arrive(&sm.full[it]);
+        // metadata of tile 0; the arrival releases it (a dropped tile's
+        // arrival only lets its bytes be waited for before the exit)
+        if (pre) {
+            if (use0)
+                stage_meta(sm, p, 0, rt0);
+            mbar_arrive(&sm.full[0]);
         }
         sm.issued = pre;
         // once the first tile is here, load the other stages (metadata, bytes
         // expected, then the arrival that releases both); a wait that gives
         // up is seen again, and handled, by the tile loop
-        if (pre == 1 && mbar_wait_bounded(&sm.full[0], 0u)) {
+        if (pre && use0 && mbar_wait_bounded(&sm.full[0], 0u)) {
             for (int n = 1; n < Sm::kNS; ++n) {
                 int rt, st;
                 if (!tile_of(p, n_units, n, rt, st))
@@ -657,8 +651,8 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     if (lane == 0)
         atomicMin(&sm.consumed, done);
     __syncthreads();
-    // never leave with a tile load still in flight (only after an abort, when
-    // warps may have stopped at different tiles)
+    // never leave with a tile load still in flight (after an abort, when
+    // warps may have stopped at different tiles, or for a dropped tile 0)
     if (threadIdx.x == 0) {
         for (int i = sm.consumed; i < sm.issued; ++i)
             (void)mbar_wait_bounded(&sm.full[i % Sm::kNS], (uint32_t)(i / Sm::kNS) & 1u);
