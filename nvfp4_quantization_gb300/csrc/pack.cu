@@ -413,7 +413,7 @@ __device__ __forceinline__ void encode_lane_blocks(const uint32_t (&w)[NB][8], c
 // the tokens are complete when this grid starts, so each warp copies and
 // encodes its first token while the routing kernel still runs, and waits for
 // it only before reading the destinations.  Otherwise nothing is read before
-// the wait but an L2 prefetch of the first tokens (it returns no data).
+// the wait but an L2 prefetch of the first two tokens (it returns no data).
 constexpr int kPackWarps = 4;
 // One buffer per warp: the next token's copy is issued as soon as the current
 // one is in registers, so it overlaps the encode and the stores; a second
@@ -439,10 +439,13 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
         return;
     }
     // Before the wait for the routing plan: pull this warp's first tokens
-    // into L2 (the ones the first bulk copies do not fetch at once)
-    if ((threadIdx.x & 31) == 0) {
+    // into L2.  Under `early` the first token's bulk copy starts at once and
+    // the next token's copy is issued as soon as the first has arrived, so
+    // nothing is prefetched (an early prefetch would only compete with the
+    // first copies).
+    if (!early && (threadIdx.x & 31) == 0) {
         const int tw = blockIdx.x * kPackWarps + (threadIdx.x >> 5);
-        for (int q = early ? kBuf : 0; q < kBuf + 1; ++q) {
+        for (int q = 0; q < kBuf + 1; ++q) {
             const int t = tw + q * n_tok_ctas * kPackWarps;
             if (t < T)
                 bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(tokens) + (int64_t)t * 2 * H, 2u * (uint32_t)H);
