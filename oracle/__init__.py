@@ -84,6 +84,7 @@ def _declare(L):
     L.or_route_plan.restype = ctypes.c_uint32
     L.or_nvfp4_pack_token.argtypes = [_P, _I64, ctypes.c_uint32, _I32, _U64, _U64, _P]
     L.or_nvfp4_pack_token.restype = None
+    L.or_scale_swizzle.argtypes = [_P, _I64, _I64, _P]; L.or_scale_swizzle.restype = None
     L.or_nvfp4_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _I32, _U64]
     L.or_nvfp4_pack.restype = None
     L.or_nvfp4_unpack.argtypes = [_P, _I64, _I64, _P, _I32, _P]
@@ -244,6 +245,41 @@ def expert_amax(rows: np.ndarray, H: int, offsets, E):
     a = np.zeros(E, np.float32); c = np.zeros(E, np.float32); s = np.zeros(E, np.float32)
     lib().or_expert_amax(_ptr(rows), H, _ptr(offsets), E, _ptr(a), _ptr(c), _ptr(s))
     return a, c, s
+
+
+def scale_swizzle(lin: np.ndarray) -> np.ndarray:
+    """Scale matrix [M, Kb] (uint8, M % 128 == 0, Kb % 4 == 0) -> its M*Kb
+    bytes in the tiled block-scaled GEMM layout (reading R23)."""
+    lin = _as(lin, np.uint8)
+    M, Kb = lin.shape
+    if M % 128 or Kb % 4:
+        raise ValueError("scale_swizzle needs M % 128 == 0 and Kb % 4 == 0")
+    out = np.zeros(M * Kb, np.uint8)
+    lib().or_scale_swizzle(_ptr(lin), M, Kb, _ptr(out))
+    return out
+
+
+def swizzle_grouped_scales(dr: dict, H: int, offsets, E) -> dict:
+    """The grouped operands of ``nvfp4_direct_receive`` with both scale
+    tensors in the tiled layout (R23): the rowwise scales of rows [0, R) as one
+    [R, H/16] matrix (expert slots are whole 128-row tiles), the columnwise
+    scales of each expert as its own [H, n_e/16] matrix at byte
+    offsets[e]*H/16.  Bytes past R*H/16 keep the linear values."""
+    offsets = _as(offsets, np.int32)
+    R = int(offsets[E])
+    out = dict(dr)
+    rw = dr["rw_scales"].copy()
+    flat = rw.reshape(-1)
+    flat[: R * H // 16] = scale_swizzle(dr["rw_scales"][:R])
+    out["rw_scales"] = rw
+    cw = dr["cw_scales"].copy()
+    for e in range(E):
+        a, n = int(offsets[e]), int(offsets[e + 1] - offsets[e])
+        if n:
+            blk = dr["cw_scales"][a * H // 16:(a + n) * H // 16].reshape(H, n // 16)
+            cw[a * H // 16:(a + n) * H // 16] = scale_swizzle(blk)
+    out["cw_scales"] = cw
+    return out
 
 
 def nvfp4_direct_receive(rows: np.ndarray, H: int, offsets, E, rounding: int = ROUND_RNE,

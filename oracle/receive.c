@@ -150,3 +150,25 @@ void or_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H,
         }
     }
 }
+
+/* Scale-factor layout of a block-scaled GEMM operand (reading R23).  TE PR
+ * #3753 "Add NVFP4 EP dispatch and combine backward", commit "... under NVFP4
+ * autocast": the combine backward returns the gradient as a "swizzled NVFP4
+ * GroupedTensor" that holds only GEMM operands; the pages do not spell the
+ * layout out.  The one taken is the tiled layout that Blackwell block-scaled
+ * matrix multiplies read: the scale matrix SF[M][Kb] (M a multiple of 128, Kb
+ * a multiple of 4) is cut into tiles of 128 rows x 4 scale columns, stored
+ * one after another with the tiles along Kb contiguous (tile (mt, kt) at
+ * (mt * Kb/4 + kt) * 512); inside a tile, element (m, kb) is at
+ *   (m mod 32) * 16 + ((m mod 128) / 32) * 4 + (kb mod 4).
+ * lin is row-major [M][Kb]; out receives the M*Kb bytes in tiled order. */
+void or_scale_swizzle(const uint8_t *lin, int64_t M, int64_t Kb, uint8_t *out)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t kb = 0; kb < Kb; ++kb) {
+            int64_t tile = (m / 128) * (Kb / 4) + kb / 4;
+            int64_t in_tile = (m % 32) * 16 + ((m % 128) / 32) * 4 + kb % 4;
+            out[tile * 512 + in_tile] = lin[m * Kb + kb];
+        }
+    }
+}
