@@ -321,9 +321,11 @@ def gpu_arm(args, rank, world, local):
 
 
 def aux_measure(torch, nq, w, b, R, reps=20):
-    """CUDA-event times of ep_nvfp4_unpack (the step's rows -> BF16) and
-    ep_mxfp8_pack (the step's tokens), each launch after a 512 MB write that
-    flushes the L2, median of ``reps``."""
+    """CUDA-event times of ep_nvfp4_unpack (the step's rows -> BF16),
+    ep_mxfp8_pack (the step's tokens) and the direct receive with both scale
+    tensors in the tiled GEMM layout and, for comparison, in the linear one
+    (the step's rows), each launch after a 512 MB write that flushes the L2,
+    median of ``reps``."""
     H, S = w.H, nq.row_bytes(w.H)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     out = torch.empty((b.plan.R_cap, H), dtype=torch.bfloat16, device="cuda")
@@ -347,8 +349,18 @@ def aux_measure(torch, nq, w, b, R, reps=20):
     ms_m = timed(lambda: nq.ep_mxfp8_pack(b.tok, b.plan, buf=mx))
     bytes_u = R * S + R * 2 * H
     bytes_m = 2 * w.T * H + 4 * w.T * w.k + R * (H + H // 32)
+    res = {"unpack": {"ms": ms_u, "bytes": bytes_u}, "mxfp8_pack": {"ms": ms_m, "bytes": bytes_m}}
+    if H % 128 == 0:
+        g = nq.alloc_grouped(b.plan.R_cap, H, w.E, "cuda")
+        bytes_d = algorithmic_bytes(w.T, H, w.k, w.E, R, S)[2]
+        for name, swz in (("direct_receive_linear", False), ("direct_receive_swizzled", True)):
+            ms = timed(lambda: nq.ep_nvfp4_direct_receive(b.rows, H, b.plan.offsets, w.E, out=g, rounding=w.rounding,
+                                                          seed=w.seed, sign_mask=w.sign_mask, status=b.plan.status,
+                                                          swizzled=swz))
+            res[name] = {"ms": ms, "bytes": bytes_d}
+        del g
     del flush, out, mx
-    return {"unpack": {"ms": ms_u, "bytes": bytes_u}, "mxfp8_pack": {"ms": ms_m, "bytes": bytes_m}}
+    return res
 
 
 def e2e_measure(torch, nq, w, bufs, tok_host, topk_host, R, steps):

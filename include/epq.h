@@ -263,6 +263,32 @@ ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
                                   void *stream);
 
 /*
+ * ep_nvfp4_direct_receive_swizzled -- ep_nvfp4_direct_receive with both scale
+ * tensors in the tiled layout that block-scaled GEMMs read.
+ * TE PR #3753, commit "... under NVFP4 autocast": the combine backward returns
+ * FC2's gradient as a "swizzled NVFP4 GroupedTensor" holding only GEMM
+ * operands.  The pages do not spell the layout out; the one used is the
+ * Blackwell block-scaled operand layout: a scale matrix SF[M][Kb] is cut into
+ * 512-byte tiles of 128 rows x 4 scale columns, tile (mt, kt) at byte
+ * (mt*Kb/4 + kt)*512, and element (m, kb) of a tile at
+ * (m mod 32)*16 + ((m mod 128)/32)*4 + (kb mod 4).
+ *   Arguments, codes, row scales, metadata and errors: as
+ *   ep_nvfp4_direct_receive, plus H % 128 != 0 -> EP_ERR_SHAPE.
+ *   rw_scales: the [R, H/16] matrix of rows [0, R) in that layout (expert
+ *   slots are whole 128-row tiles); bytes past R*H/16 are left untouched.
+ *   cw_scales: expert e's [H, n_e/16] matrix in that layout, at byte
+ *   offsets[e]*H/16 (the same place and size as the linear form).
+ */
+ep_status ep_nvfp4_direct_receive_swizzled(const uint8_t *rows, int64_t R_cap,
+                                           int64_t H,
+                                           const int32_t *expert_offsets,
+                                           int E, const ep_nvfp4_grouped *out,
+                                           int rounding, uint64_t seed,
+                                           uint16_t rht_sign_mask,
+                                           uint32_t *dev_status,
+                                           void *stream);
+
+/*
  * ep_mxfp8_pack -- MXFP8 variant of the pack with the same routing gather.
  * TE PR #3270, description: bfloat16 tokens are quantised to MXFP8 and
  * dispatched; sequence diagram: "Quantize to E4M3 + E8M0 scales"; Changes:

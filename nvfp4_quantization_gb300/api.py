@@ -196,9 +196,11 @@ def grouped_struct(g: dict) -> EpGrouped:
 def ep_nvfp4_direct_receive(rows: torch.Tensor, H: int, offsets: torch.Tensor, E: int,
                             out: dict | None = None, rounding: int = EP_ROUND_RNE, seed: int = 0,
                             sign_mask: int = DEFAULT_SIGN_MASK, status: torch.Tensor | None = None,
-                            rowwise: bool = True, stream=None) -> dict:
+                            rowwise: bool = True, swizzled: bool = False, stream=None) -> dict:
     """Packed rows -> grouped rowwise + columnwise-RHT NVFP4 operands (dict of
-    tensors, see ep_nvfp4_grouped in include/epq.h)."""
+    tensors, see ep_nvfp4_grouped in include/epq.h).  ``swizzled`` calls
+    ep_nvfp4_direct_receive_swizzled: both scale tensors in the tiled layout
+    of block-scaled GEMM operands (H % 128 == 0)."""
     _need_cuda(rows, "rows", torch.uint8)
     R_cap = rows.shape[0]
     if out is None:
@@ -206,10 +208,11 @@ def ep_nvfp4_direct_receive(rows: torch.Tensor, H: int, offsets: torch.Tensor, E
     if status is None:
         status = new_status(rows.device)
     desc = grouped_struct(out)
-    st = _lib.lib().ep_nvfp4_direct_receive(_ptr(rows), R_cap, H, _ptr(offsets), E, ctypes.byref(desc),
-                                            int(rounding), int(seed) & ((1 << 64) - 1), int(sign_mask) & 0xFFFF,
-                                            _ptr(status), _stream(stream))
-    check("ep_nvfp4_direct_receive", st)
+    name = "ep_nvfp4_direct_receive_swizzled" if swizzled else "ep_nvfp4_direct_receive"
+    st = getattr(_lib.lib(), name)(_ptr(rows), R_cap, H, _ptr(offsets), E, ctypes.byref(desc), int(rounding),
+                                   int(seed) & ((1 << 64) - 1), int(sign_mask) & 0xFFFF, _ptr(status),
+                                   _stream(stream))
+    check(name, st)
     return out
 
 

@@ -251,9 +251,10 @@ ep_status ep_nvfp4_unpack(const uint8_t *rows, int64_t R_cap, int64_t H, const i
                                                 (uint16_t *)out_bf16, dev_status));
 }
 
-ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H, const int32_t *expert_offsets,
-                                  int E, const ep_nvfp4_grouped *out, int rounding, uint64_t seed,
-                                  uint16_t rht_sign_mask, uint32_t *dev_status, void *stream)
+static ep_status direct_receive_common(const uint8_t *rows, int64_t R_cap, int64_t H,
+                                       const int32_t *expert_offsets, int E, const ep_nvfp4_grouped *out,
+                                       int rounding, uint64_t seed, uint16_t rht_sign_mask, uint32_t *dev_status,
+                                       void *stream, bool swz)
 {
     if (!rows || !expert_offsets || !out || !dev_status)
         return EP_ERR_NULL;
@@ -263,7 +264,7 @@ ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H,
     const bool rw_all = out->rw_codes && out->rw_scales && out->rw_row_scale;
     if (rw_any && !rw_all)
         return EP_ERR_NULL;
-    if (!shape_ok(0, H, 1, E))
+    if (!shape_ok(0, H, 1, E) || (swz && H % 128 != 0))
         return EP_ERR_SHAPE;
     if (R_cap < 0 || R_cap > (int64_t)INT32_MAX)
         return EP_ERR_CAPACITY;
@@ -285,7 +286,24 @@ ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H,
     epq::GroupedOut o{out->rw_codes, out->rw_scales, out->rw_row_scale, out->cw_codes,
                       out->cw_scales, out->amax_row, out->amax_col, out->cw_scale_enc};
     return cuda_status(epq::launch_direct_receive(c, rows, (int)R_cap, (int)H, expert_offsets, E, o, rounding,
-                                                  seed, rht_sign_mask, dev_status));
+                                                  seed, rht_sign_mask, dev_status, swz));
+}
+
+ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H, const int32_t *expert_offsets,
+                                  int E, const ep_nvfp4_grouped *out, int rounding, uint64_t seed,
+                                  uint16_t rht_sign_mask, uint32_t *dev_status, void *stream)
+{
+    return direct_receive_common(rows, R_cap, H, expert_offsets, E, out, rounding, seed, rht_sign_mask, dev_status,
+                                 stream, false);
+}
+
+ep_status ep_nvfp4_direct_receive_swizzled(const uint8_t *rows, int64_t R_cap, int64_t H,
+                                           const int32_t *expert_offsets, int E, const ep_nvfp4_grouped *out,
+                                           int rounding, uint64_t seed, uint16_t rht_sign_mask,
+                                           uint32_t *dev_status, void *stream)
+{
+    return direct_receive_common(rows, R_cap, H, expert_offsets, E, out, rounding, seed, rht_sign_mask, dev_status,
+                                 stream, true);
 }
 
 } // extern "C"

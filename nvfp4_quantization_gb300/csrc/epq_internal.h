@@ -84,10 +84,12 @@ struct GroupedOut {
     float *scale_enc;
 };
 
+// swz: both scale tensors in the tiled layout of block-scaled GEMM operands
+// (H % 128 == 0, checked by the caller).
 cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
                                   const int32_t *offsets, int E, const GroupedOut &out,
                                   int rounding, uint64_t seed, uint32_t sign_mask,
-                                  uint32_t *status);
+                                  uint32_t *status, bool swz = false);
 
 // Bytes of a packed NVFP4 row: roundup16(9H/16 + 16).
 inline int64_t row_bytes(int64_t H) { return (9 * H / 16 + 16 + 15) / 16 * 16; }

@@ -340,7 +340,7 @@ __device__ __forceinline__ void rht_block(const Sm &sm, int s, const void *tab, 
                      cvt_e2m1x8(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y));
 }
 
-template <bool kSR, class Sm>
+template <bool kSR, bool kSwz, class Sm>
 __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, const CUtensorMap *tm_rws,
                                              const CUtensorMap *tmc, const CUtensorMap *tms,
                                              const CUtensorMap *tmt, const DrArgs &p, int n_units)
@@ -377,7 +377,7 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
                     tma_store_2d(tm_rws, st * kScaleBytes, row0, &sm.scales[s][0][0]);
                 tma_store_commit();
             }
-            if (!p.rws_tma) {
+            if (!p.rws_tma && !kSwz) {
                 const int nb = min(kScaleBytes, H / 16 - st * kScaleBytes);
                 uint8_t *dst = p.rw_scales + (int64_t)(row0 + c) * (H / 16) + st * kScaleBytes;
                 const uint8_t *src = &sm.scales[s][c][0];
@@ -386,6 +386,22 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
             }
             if (st == 0)
                 p.rw_row_scale[row0 + c] = u2f(sm.trailer[s][c][0]);
+        }
+        if (p.do_rowwise && kSwz) {
+            // tiled layout: the strip's scale columns 16 st .. 16 st + 15 of
+            // rows row0 .. row0 + 127 are the 512-byte tiles (rt, 4 st + g),
+            // g = 0..3, one contiguous run; word (g, i, q) of the run (i =
+            // row mod 32, q = row / 32) holds the 4 scale bytes of group g of
+            // row 32 q + i
+            const int ng = min(4, (H / 16 - st * kScaleBytes) / 4);
+            uint8_t *run = p.rw_scales + ((int64_t)rt * (H / 64) + 4 * st) * 512;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int w = c + kThreads * j, g = w >> 7, i = (w >> 2) & 31, q = w & 3;
+                if (g < ng)
+                    *reinterpret_cast<uint32_t *>(run + 4 * w) =
+                        *reinterpret_cast<const uint32_t *>(&sm.scales[s][32 * q + i][4 * g]);
+            }
         }
 
         // this warp's decode scales: rows 64 hh + {lane, lane + 32}, column
@@ -496,12 +512,20 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
                 st16g(d1, q1[0]);
                 st16g(d1 + 16, q1[1]);
             }
+            // tiled layout: this warp's 4 scale bytes of a column are one word
+            // of the expert's tile (column / 128, row-in-expert / 64)
+            if (kSwz) {
+                uint8_t *t = p.cw_scales + (int64_t)m.off * (H / 16) +
+                             ((int64_t)(h0 >> 7) * (m.n / 64) + (rl + 64 * hh) / 64) * 512 + ((h0 & 127) >> 5) * 4;
+                *reinterpret_cast<uint32_t *>(t + (h0 & 31) * 16) = sc0;
+                *reinterpret_cast<uint32_t *>(t + ((h0 + 1) & 31) * 16) = sc1;
+            }
             // rows 64..127 hand their scale bytes to the warp holding rows
             // 0..63 of the same columns, so each column's 8 scale bytes of
             // the tile leave in one store (the stage's reuse orders the
             // buffer: the producer refills stage s only after both warps
             // released it)
-            if (hh == 1) {
+            else if (hh == 1) {
                 sm.csc[s][cq][lane][0] = sc0;
                 sm.csc[s][cq][lane][1] = sc1;
             } else {
@@ -509,7 +533,8 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
                 csc1 = sc1;
             }
         }
-        if (hh == 1) {
+        if (kSwz) {
+        } else if (hh == 1) {
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.csc_full[s][cq]);
@@ -559,7 +584,8 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
     return done;
 }
 
-template <bool kSR>
+// kSwz: both scale tensors in the tiled layout of block-scaled GEMM operands.
+template <bool kSR, bool kSwz>
 __global__ void __launch_bounds__(kThreads, DrCfg<kSR>::kCtasPerSm)
 direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
                       const __grid_constant__ CUtensorMap tm_scales,
@@ -647,7 +673,7 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         }
     }
 
-    const int done = consumer_loop<kSR>(sm, &tm_rw, &tm_rws, &tm_codes, &tm_scales, &tm_trailer, p, n_units);
+    const int done = consumer_loop<kSR, kSwz>(sm, &tm_rw, &tm_rws, &tm_codes, &tm_scales, &tm_trailer, p, n_units);
     if (lane == 0)
         atomicMin(&sm.consumed, done);
     __syncthreads();
@@ -693,7 +719,7 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
 cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
                                   const int32_t *offsets, int E, const GroupedOut &out,
                                   int rounding, uint64_t seed, uint32_t sign_mask,
-                                  uint32_t *status)
+                                  uint32_t *status, bool swz)
 {
     const int64_t S = row_bytes(H);
     cudaError_t err = launch_pdl(expert_amax_kernel, dim3((unsigned)E), dim3(kAmaxThreads), 0, c.stream, rows, S,
@@ -714,7 +740,7 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
         return cudaErrorInvalidValue;
     // rowwise scales by TMA when every strip is a whole 16-byte box and the
     // row pitch H/16 is a multiple of 16 bytes
-    const int rws_tma = do_rw && H % kTileCols == 0 &&
+    const int rws_tma = do_rw && !swz && H % kTileCols == 0 &&
                         make_map(&tm_rws, out.rw_scales, (uint64_t)H / 16, rc, (uint64_t)H / 16, kScaleBytes, kTileRows);
 
     DrArgs a;
@@ -744,9 +770,10 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
 
     const bool sr = rounding == 1;
     const size_t smem = (sr ? sizeof(DrCfg<true>::Smem) : sizeof(DrCfg<false>::Smem)) + 1024;
-    static int done_rn[2] = {0, 0}, done_sr[2] = {0, 0};
-    err = sr ? ensure_smem_limit(direct_receive_kernel<true>, c.device, (int)smem, done_sr)
-             : ensure_smem_limit(direct_receive_kernel<false>, c.device, (int)smem, done_rn);
+    static int done[4][2] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}};
+    auto kern = sr ? (swz ? direct_receive_kernel<true, true> : direct_receive_kernel<true, false>)
+                   : (swz ? direct_receive_kernel<false, true> : direct_receive_kernel<false, false>);
+    err = ensure_smem_limit(kern, c.device, (int)smem, done[(sr ? 2 : 0) + (swz ? 1 : 0)]);
     if (err != cudaSuccess)
         return err;
     const int64_t max_units = (int64_t)(R_cap / kTileRows) * a.n_strips;
@@ -755,11 +782,8 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
         grid = max_units;
     if (grid < 1)
         grid = 1;
-    if (rounding == 1)
-        return launch_pdl(direct_receive_kernel<true>, dim3((unsigned)grid), dim3(kThreads), smem, c.stream,
-                          tm_codes, tm_scales, tm_trailer, tm_rw, tm_rws, a);
-    return launch_pdl(direct_receive_kernel<false>, dim3((unsigned)grid), dim3(kThreads), smem, c.stream, tm_codes,
-                      tm_scales, tm_trailer, tm_rw, tm_rws, a);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, c.stream, tm_codes, tm_scales, tm_trailer,
+                      tm_rw, tm_rws, a);
 }
 
 } // namespace epq

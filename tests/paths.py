@@ -30,8 +30,9 @@ def assert_bytes_equal(got: np.ndarray, want: np.ndarray, what: str):
 class GpuRun:
     """The hot path on the GPU for one workload, with canary-filled outputs."""
 
-    def __init__(self, w, rowwise=True, mxfp8=False, unpack=False, R_cap=None, dispatch=False):
+    def __init__(self, w, rowwise=True, mxfp8=False, unpack=False, R_cap=None, dispatch=False, swizzled=False):
         self.w = w
+        self.swizzled = swizzled
         self.tok = to_dev_bf16(w.tokens)
         self.topk = torch.from_numpy(np.ascontiguousarray(w.topk)).cuda()
         self.R_cap = R_cap or nq.rows_capacity(w.T, w.k, w.E, w.A)
@@ -48,7 +49,7 @@ class GpuRun:
             t.view(torch.uint8).fill_(CANARY)
         self.grouped = nq.ep_nvfp4_direct_receive(self.rows, w.H, self.plan.offsets, w.E, out=g,
                                                   rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask,
-                                                  status=self.plan.status)
+                                                  status=self.plan.status, swizzled=swizzled)
         self.unpacked = None
         if unpack:
             self.unpacked = torch.full((self.R_cap, w.H), 0, dtype=torch.bfloat16, device="cuda")
@@ -93,16 +94,18 @@ def compare_runs(g: GpuRun, o: OracleRun, check_rowwise=True):
     assert_bytes_equal(rows[:R], o.rows[:R], "packed rows")
     assert (rows[R:] == CANARY).all(), "rows beyond R were written"
     gr = {k: g.host(v) for k, v in g.grouped.items()}
+    odr = oracle.swizzle_grouped_scales(o.dr, H, o.off, w.E) if g.swizzled else o.dr
     for name in ("amax_row", "amax_col", "cw_scale_enc"):
         oname = "scale_enc" if name == "cw_scale_enc" else name
         assert_bytes_equal(gr[name].view(np.uint32), o.dr[oname].view(np.uint32), name)
     assert_bytes_equal(gr["cw_codes"][: R * H // 2], o.dr["cw_codes"][: R * H // 2], "columnwise codes")
-    assert_bytes_equal(gr["cw_scales"][: R * H // 16], o.dr["cw_scales"][: R * H // 16], "columnwise scales")
+    assert_bytes_equal(gr["cw_scales"][: R * H // 16], odr["cw_scales"][: R * H // 16], "columnwise scales")
     assert (gr["cw_codes"][R * H // 2:] == CANARY).all()
     assert (gr["cw_scales"][R * H // 16:] == CANARY).all()
     if check_rowwise and "rw_codes" in gr:
         assert_bytes_equal(gr["rw_codes"][:R], o.dr["rw_codes"][:R], "rowwise codes")
-        assert_bytes_equal(gr["rw_scales"][:R], o.dr["rw_scales"][:R], "rowwise scales")
+        assert_bytes_equal(gr["rw_scales"][:R], odr["rw_scales"][:R], "rowwise scales")
+        assert (gr["rw_scales"][R:] == CANARY).all()
         assert_bytes_equal(gr["rw_row_scale"][:R].view(np.uint32), o.dr["rw_row_scale"][:R].view(np.uint32),
                            "rowwise row scale")
         assert (gr["rw_codes"][R:] == CANARY).all()

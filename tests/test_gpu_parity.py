@@ -56,6 +56,28 @@ def test_parity_dispatch_sr_many_tokens_per_warp():
     compare_runs(g, o)
 
 
+@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg4", "cfg5"])
+def test_parity_swizzled_scales(name):
+    """ep_nvfp4_direct_receive_swizzled: codes, row scales and metadata as the
+    linear call, both scale tensors equal to the oracle's scales put in the
+    tiled layout (rowwise over rows [0, R), columnwise per expert)."""
+    c = CASES[name]
+    w = workloads.make(c["cfg"], **c["kw"])
+    g = GpuRun(w, swizzled=True)
+    o = OracleRun(w, g.R_cap)
+    compare_runs(g, o)
+
+
+def test_swizzled_scales_need_h_multiple_of_128():
+    w = workloads.make(1, T=64, H=1056)
+    tok = to_dev_bf16(w.tokens)
+    plan = nq.ep_route_plan(torch.from_numpy(w.topk).cuda(), w.E, w.A)
+    rows = nq.ep_nvfp4_pack(tok, plan)
+    with pytest.raises(nq.EpError) as ei:
+        nq.ep_nvfp4_direct_receive(rows, w.H, plan.offsets, w.E, status=plan.status, swizzled=True)
+    assert ei.value.status == -2
+
+
 def test_parity_rne_and_sr_on_same_tokens():
     base = workloads.make(4, T=200, H=512, E=16, k=4)
     for rounding, seed in ((0, 0), (1, 1), (1, 0xFFFFFFFFFFFF1234)):
