@@ -85,6 +85,8 @@ def _declare(L):
     L.or_nvfp4_pack_token.argtypes = [_P, _I64, ctypes.c_uint32, _I32, _U64, _U64, _P]
     L.or_nvfp4_pack_token.restype = None
     L.or_scale_swizzle.argtypes = [_P, _I64, _I64, _P]; L.or_scale_swizzle.restype = None
+    L.or_nvfp4_colwise_rht_bf16.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _P, _I32, _U64, _U16, _P]
+    L.or_nvfp4_colwise_rht_bf16.restype = None
     L.or_nvfp4_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _I32, _U64]
     L.or_nvfp4_pack.restype = None
     L.or_nvfp4_unpack.argtypes = [_P, _I64, _I64, _P, _I32, _P]
@@ -314,6 +316,26 @@ def nvfp4_direct_receive(rows: np.ndarray, H: int, offsets, E, rounding: int = R
         _ptr(out["cw_codes"]), _ptr(out["cw_scales"]), _ptr(out["amax_row"]),
         _ptr(out["amax_col"]), _ptr(out["scale_enc"]), rounding, seed, sign_mask,
         _ptr(report))
+    out["report"] = dict(scale_saturated=int(report[0]), above_4x_rowwise_amax=int(report[1]),
+                         element_saturated=int(report[2]), above_4x_block_input=int(report[3]))
+    return out
+
+
+def nvfp4_colwise_rht_bf16(x_bf16: np.ndarray, offsets, E, amax_in, rounding: int = ROUND_RNE, seed: int = 0,
+                           sign_mask: int = DEFAULT_SIGN_MASK) -> dict:
+    """BF16 rows [R_cap, H] (expert-grouped) + supplied per-expert amax ->
+    the columnwise RHT operand and the per-expert metadata (reading R24)."""
+    x = _as(x_bf16, np.uint16)
+    R_cap, H = x.shape
+    offsets = _as(offsets, np.int32)
+    amax_in = _as(amax_in, np.float32)
+    out = dict(cw_codes=np.zeros(R_cap * H // 2, np.uint8), cw_scales=np.zeros(R_cap * H // 16, np.uint8),
+               amax_row=np.zeros(E, np.float32), amax_col=np.zeros(E, np.float32),
+               scale_enc=np.zeros(E, np.float32))
+    report = np.zeros(4, np.int64)
+    lib().or_nvfp4_colwise_rht_bf16(_ptr(x), R_cap, H, _ptr(offsets), E, _ptr(amax_in), _ptr(out["cw_codes"]),
+                                    _ptr(out["cw_scales"]), _ptr(out["amax_row"]), _ptr(out["amax_col"]),
+                                    _ptr(out["scale_enc"]), rounding, seed, sign_mask, _ptr(report))
     out["report"] = dict(scale_saturated=int(report[0]), above_4x_rowwise_amax=int(report[1]),
                          element_saturated=int(report[2]), above_4x_block_input=int(report[3]))
     return out

@@ -93,6 +93,16 @@ void     or_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H,
                                  float *amax_col, float *scale_enc,
                                  int rounding, uint64_t seed,
                                  uint16_t sign_mask, int64_t *report);
+/* BF16-input columnwise RHT operand with a supplied per-expert amax (R24);
+ * report as for or_nvfp4_direct_receive (report[1]: values above 4 x the
+ * rounded supplied amax). */
+void     or_nvfp4_colwise_rht_bf16(const uint16_t *x, int64_t R_cap, int64_t H,
+                                   const int32_t *offsets, int E,
+                                   const float *amax_in, uint8_t *cw_codes,
+                                   uint8_t *cw_scales, float *amax_row,
+                                   float *amax_col, float *scale_enc,
+                                   int rounding, uint64_t seed,
+                                   uint16_t sign_mask, int64_t *report);
 /* Tiled scale-factor layout (R23): M % 128 == 0, Kb % 4 == 0. */
 void     or_scale_swizzle(const uint8_t *lin, int64_t M, int64_t Kb, uint8_t *out);
 void     or_mxfp8_pack(const uint16_t *tokens, int64_t T, int64_t H,

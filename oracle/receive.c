@@ -172,3 +172,98 @@ void or_scale_swizzle(const uint8_t *lin, int64_t M, int64_t Kb, uint8_t *out)
         }
     }
 }
+
+/* Columnwise RHT operand of a BF16 input with a supplied per-expert amax
+ * (reading R24).  TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the
+ * dGLU epilogue", PR description: the rowwise amax is the exact amax of the
+ * dGLU epilogue rounded to BF16, the post-RHT columnwise amax is bounded by 4x
+ * the rowwise amax, and the separate grouped amax pass is skipped.
+ *   x        BF16 [R_cap][H], rows in expert order (expert e: rows
+ *            [offsets[e], offsets[e+1]), a multiple of 16 rows)
+ *   amax_in  [E] the supplied amax of each expert
+ * Per expert: amax_row = BF16_RNE(amax_in), amax_col = fl32(4 amax_row),
+ * S_enc as for the direct receive (R11).  Per hidden column and block of 16
+ * consecutive rows: d = the BF16 values (exact in float), the same RHT,
+ * block scale and codes as the direct receive's columnwise operand (R9, R11,
+ * R12); stochastic rounding draws from Philox stream 2 with element index
+ * off*H + h*n + row-in-expert (R13). */
+void or_nvfp4_colwise_rht_bf16(const uint16_t *x, int64_t R_cap, int64_t H,
+                               const int32_t *offsets, int E,
+                               const float *amax_in, uint8_t *cw_codes,
+                               uint8_t *cw_scales, float *amax_row,
+                               float *amax_col, float *scale_enc,
+                               int rounding, uint64_t seed,
+                               uint16_t sign_mask, int64_t *report)
+{
+    (void)R_cap;
+    for (int i = 0; i < 4; ++i)
+        report[i] = 0;
+    for (int e = 0; e < E; ++e) {
+        uint16_t ab = or_bf16_rne((double)amax_in[e]);
+        uint32_t bits = (uint32_t)ab << 16;
+        float a;
+        memcpy(&a, &bits, 4);
+        float ac = 4.0f * a;
+        float se = 1.0f;
+        if (ac > 0.0f) {
+            se = 2688.0f / ac;
+            if (se > FLT_MAX)
+                se = FLT_MAX;
+        }
+        amax_row[e] = a;
+        amax_col[e] = ac;
+        scale_enc[e] = se;
+
+        int64_t off = offsets[e];
+        int64_t n = offsets[e + 1] - offsets[e];
+        float ce = se / 6.0f;
+        uint8_t *cc = cw_codes + (size_t)off * (size_t)(H / 2);
+        uint8_t *cs = cw_scales + (size_t)off * (size_t)(H / 16);
+        for (int64_t h = 0; h < H; ++h) {
+            for (int64_t j = 0; j < n / 16; ++j) {
+                float d[16], y[16];
+                float dmax = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    uint32_t b = (uint32_t)x[(size_t)(off + 16 * j + i) * (size_t)H + (size_t)h] << 16;
+                    memcpy(&d[i], &b, 4);
+                    dmax = fmaxf(dmax, fabsf(d[i]));
+                }
+                or_rht16_f32(d, sign_mask, y);
+                float bmax = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    float ay = fabsf(y[i]);
+                    bmax = fmaxf(bmax, ay);
+                    if (ay > ac)
+                        report[1] += 1;
+                    if (ay > 4.0f * dmax)
+                        report[3] += 1;
+                }
+                float sprod = bmax * ce;
+                int s = or_e4m3_rne_sat((double)sprod);
+                if ((double)sprod > 448.0)
+                    report[0] += 1;
+                float sval = (float)or_e4m3_value(s);
+                float r = (sval == 0.0f) ? 0.0f : se / sval;
+                cs[h * (n / 16) + j] = (uint8_t)s;
+                for (int i = 0; i < 16; ++i) {
+                    float v = fabsf(y[i]) * r;
+                    if (v > 6.0f)
+                        report[2] += 1;
+                    double sv = signbit(y[i]) ? -(double)v : (double)v;
+                    int64_t pos = 16 * j + i; /* row within the expert */
+                    int code;
+                    if (rounding == 1)
+                        code = or_e2m1_sr(sv, or_sr_byte(seed, 2u,
+                                   (uint64_t)off * (uint64_t)H + (uint64_t)h * (uint64_t)n + (uint64_t)pos));
+                    else
+                        code = or_e2m1_rne(sv);
+                    size_t byte = (size_t)h * (size_t)(n / 2) + (size_t)(pos / 2);
+                    if (pos % 2 == 0)
+                        cc[byte] = (uint8_t)((cc[byte] & 0xf0) | code);
+                    else
+                        cc[byte] = (uint8_t)((cc[byte] & 0x0f) | (code << 4));
+                }
+            }
+        }
+    }
+}
