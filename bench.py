@@ -364,6 +364,19 @@ def aux_measure(torch, nq, w, b, R, reps=20):
     bytes_u = R * S + R * 2 * H
     bytes_m = 2 * w.T * H + 4 * w.T * w.k + R * (H + H // 32)
     res = {"unpack": {"ms": ms_u, "bytes": bytes_u}, "mxfp8_pack": {"ms": ms_m, "bytes": bytes_m}}
+    # the columnwise RHT operand of the decoded rows (BF16) with the supplied
+    # per-expert amax (the dGLU-epilogue path): the rows unpacked above, the
+    # step's own rowwise amaxes
+    cw = {"cw_codes": torch.empty(b.plan.R_cap * H // 2, dtype=torch.uint8, device="cuda"),
+          "cw_scales": torch.empty(b.plan.R_cap * H // 16, dtype=torch.uint8, device="cuda"),
+          "amax_row": torch.empty(w.E, dtype=torch.float32, device="cuda"),
+          "amax_col": torch.empty(w.E, dtype=torch.float32, device="cuda"),
+          "cw_scale_enc": torch.empty(w.E, dtype=torch.float32, device="cuda")}
+    ms_c = timed(lambda: nq.ep_nvfp4_colwise_rht_bf16(out, b.plan.offsets, w.E, b.out["amax_row"], out=cw,
+                                                      rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask,
+                                                      status=b.plan.status))
+    res["colwise_rht_bf16"] = {"ms": ms_c, "bytes": R * H * 2 + R * (9 * H // 16) + 16 * w.E}
+    del cw
     if H % 128 == 0:
         g = nq.alloc_grouped(b.plan.R_cap, H, w.E, "cuda")
         bytes_d = algorithmic_bytes(w.T, H, w.k, w.E, R, S)[2]

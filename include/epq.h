@@ -289,6 +289,38 @@ ep_status ep_nvfp4_direct_receive_swizzled(const uint8_t *rows, int64_t R_cap,
                                            void *stream);
 
 /*
+ * ep_nvfp4_colwise_rht_bf16 -- the columnwise RHT operand of an expert-grouped
+ * BF16 tensor, with the per-expert amax supplied by its producer.
+ * TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the dGLU epilogue",
+ * PR description: "the rowwise amax is the exact dGLU epilogue amax rounded
+ * to BF16; the post-RHT columnwise amax is bounded by 4x the rowwise amax;
+ * skips the separate grouped amax pass".
+ *   x_bf16          device bf16 [R_cap, H], rows in expert order: expert e
+ *                   owns rows [expert_offsets[e], expert_offsets[e+1]), a
+ *                   whole number of 128-row tiles (as ep_route_plan gives);
+ *                   a slot that is not raises EP_DEV_ERR_BAD_EXPERT and its
+ *                   rows are skipped.  Finite values.
+ *   amax_in         device f32 [E]: the supplied amax of each expert.
+ *   cw_codes, cw_scales, amax_row, amax_col, cw_scale_enc: as the columnwise
+ *                   part of ep_nvfp4_grouped (layout R12: expert e's codes
+ *                   [H][n_e/2] at byte offsets[e]*H/2, scales [H][n_e/16] at
+ *                   byte offsets[e]*H/16).
+ * Per expert: amax_row = BF16_RNE(amax_in), amax_col = 4*amax_row, S_enc =
+ * min(2688/amax_col, FLT_MAX) (1 if 0).  Per hidden column and block of 16
+ * rows: the same transform, block scale and codes as the direct receive's
+ * columnwise operand with the BF16 values as input; SR draws from Philox
+ * stream 2 (counter as for the direct receive).  The data is read once.
+ */
+ep_status ep_nvfp4_colwise_rht_bf16(const void *x_bf16, int64_t R_cap,
+                                    int64_t H, const int32_t *expert_offsets,
+                                    int E, const float *amax_in,
+                                    uint8_t *cw_codes, uint8_t *cw_scales,
+                                    float *amax_row, float *amax_col,
+                                    float *cw_scale_enc, int rounding,
+                                    uint64_t seed, uint16_t rht_sign_mask,
+                                    uint32_t *dev_status, void *stream);
+
+/*
  * ep_mxfp8_pack -- MXFP8 variant of the pack with the same routing gather.
  * TE PR #3270, description: bfloat16 tokens are quantised to MXFP8 and
  * dispatched; sequence diagram: "Quantize to E4M3 + E8M0 scales"; Changes:

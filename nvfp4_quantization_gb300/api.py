@@ -216,6 +216,33 @@ def ep_nvfp4_direct_receive(rows: torch.Tensor, H: int, offsets: torch.Tensor, E
     return out
 
 
+def ep_nvfp4_colwise_rht_bf16(x: torch.Tensor, offsets: torch.Tensor, E: int, amax: torch.Tensor,
+                              out: dict | None = None, rounding: int = EP_ROUND_RNE, seed: int = 0,
+                              sign_mask: int = DEFAULT_SIGN_MASK, status: torch.Tensor | None = None,
+                              stream=None) -> dict:
+    """Expert-grouped BF16 rows [R_cap, H] + supplied per-expert amax [E]
+    (f32) -> the columnwise RHT operand and its metadata (keys cw_codes,
+    cw_scales, amax_row, amax_col, cw_scale_enc)."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(amax, "amax", torch.float32)
+    R_cap, H = x.shape
+    dev = x.device
+    if out is None:
+        out = {"cw_codes": torch.empty(R_cap * H // 2, dtype=torch.uint8, device=dev),
+               "cw_scales": torch.empty(R_cap * H // 16, dtype=torch.uint8, device=dev),
+               "amax_row": torch.empty(E, dtype=torch.float32, device=dev),
+               "amax_col": torch.empty(E, dtype=torch.float32, device=dev),
+               "cw_scale_enc": torch.empty(E, dtype=torch.float32, device=dev)}
+    if status is None:
+        status = new_status(dev)
+    st = _lib.lib().ep_nvfp4_colwise_rht_bf16(_ptr(x), R_cap, H, _ptr(offsets), E, _ptr(amax), _ptr(out["cw_codes"]),
+                                              _ptr(out["cw_scales"]), _ptr(out["amax_row"]), _ptr(out["amax_col"]),
+                                              _ptr(out["cw_scale_enc"]), int(rounding), int(seed) & ((1 << 64) - 1),
+                                              int(sign_mask) & 0xFFFF, _ptr(status), _stream(stream))
+    check("ep_nvfp4_colwise_rht_bf16", st)
+    return out
+
+
 def ep_mxfp8_pack(tokens: torch.Tensor, plan: RoutePlan, buf: torch.Tensor | None = None,
                   stream=None) -> torch.Tensor:
     """BF16 tokens -> one uint8 buffer: data [R_cap, H] then scales [R_cap, H/32]."""

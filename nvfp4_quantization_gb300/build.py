@@ -18,7 +18,7 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = BUILD / "libepq.so"
-SOURCES = ["api.cu", "route.cu", "route_noalloc.cu", "pack.cu", "unpack.cu", "receive.cu"]
+SOURCES = ["api.cu", "route.cu", "route_noalloc.cu", "pack.cu", "unpack.cu", "receive.cu", "colwise_bf16.cu"]
 HEADERS = ["epq_device.cuh", "epq_internal.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -212,6 +212,36 @@ ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16, in
     return cuda_status(err);
 }
 
+ep_status ep_nvfp4_colwise_rht_bf16(const void *x_bf16, int64_t R_cap, int64_t H, const int32_t *expert_offsets,
+                                    int E, const float *amax_in, uint8_t *cw_codes, uint8_t *cw_scales,
+                                    float *amax_row, float *amax_col, float *cw_scale_enc, int rounding,
+                                    uint64_t seed, uint16_t rht_sign_mask, uint32_t *dev_status, void *stream)
+{
+    if (!x_bf16 || !expert_offsets || !amax_in || !cw_codes || !cw_scales || !amax_row || !amax_col ||
+        !cw_scale_enc || !dev_status)
+        return EP_ERR_NULL;
+    if (!shape_ok(0, H, 1, E))
+        return EP_ERR_SHAPE;
+    if (R_cap < 0 || R_cap > (int64_t)INT32_MAX || R_cap * H / 2 > (int64_t)INT32_MAX * 16)
+        return EP_ERR_CAPACITY;
+    if (rounding != EP_ROUND_RNE && rounding != EP_ROUND_SR)
+        return EP_ERR_ARG;
+    if (!aligned16(x_bf16) || !aligned16(cw_codes) || !aligned16(cw_scales))
+        return EP_ERR_ALIGN;
+    const int dev = device_of(x_bf16);
+    if (dev < 0 || !on_device(expert_offsets, dev) || !on_device(amax_in, dev) || !on_device(cw_codes, dev) ||
+        !on_device(cw_scales, dev) || !on_device(amax_row, dev) || !on_device(amax_col, dev) ||
+        !on_device(cw_scale_enc, dev) || !on_device(dev_status, dev))
+        return EP_ERR_DEVICE;
+    DeviceGuard g(dev);
+    if (!g.ok)
+        return EP_ERR_DEVICE;
+    LaunchCtx c{(cudaStream_t)stream, dev, sm_count(dev)};
+    return cuda_status(epq::launch_colwise_rht_bf16(c, (const uint16_t *)x_bf16, (int)R_cap, (int)H, expert_offsets,
+                                                    E, amax_in, cw_codes, cw_scales, amax_row, amax_col,
+                                                    cw_scale_enc, rounding, seed, rht_sign_mask, dev_status));
+}
+
 ep_status ep_mxfp8_pack(const void *tokens_bf16, int64_t T, int64_t H, const int32_t *dest, int k,
                         const int32_t *expert_offsets, const int32_t *expert_counts, int E, uint8_t *buf,
                         int64_t R_cap, uint32_t *dev_status, void *stream)

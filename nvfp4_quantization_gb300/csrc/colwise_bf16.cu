@@ -1,0 +1,234 @@
+// Columnwise RHT operand of a BF16 input with a supplied per-expert amax.
+//
+// TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the dGLU epilogue",
+// PR description: the rowwise amax is the exact amax of the dGLU epilogue
+// rounded to BF16, the post-RHT columnwise amax is bounded by 4x the rowwise
+// amax, and the separate grouped amax pass is skipped.  The input is the
+// expert-grouped BF16 gradient; the per-expert encode scale comes from the
+// supplied amax, so the data is read once.
+//
+// Work unit of a warp: 64 rows x 16 columns of one expert (expert slots are
+// multiples of 128 rows).  Lane l takes the column pair 8 c + l/4 and the
+// 16-row block l mod 4: it loads 16 rows x 4 bytes (a warp's load is four
+// 32-byte row segments), runs the 16-point transform on FP32 pairs, derives
+// the E4M3 block scales from S_enc and writes 8 code bytes per column, so the
+// four lanes of a column fill one 32-byte sector; the 4 scale bytes of a
+// column's 64 rows are gathered by shuffles into one 4-byte store.  The same
+// arithmetic, in the same order, as the direct receive's columnwise operand,
+// with the BF16 values as the decoded input.
+#include <float.h>
+
+#include "epq_device.cuh"
+#include "epq_internal.h"
+
+namespace epq {
+
+constexpr int kCbThreads = 256;
+constexpr int kCbMaxExperts = 1024;
+
+struct CbRcp {
+    float v[128];   // RN(1 / s) for every E4M3 code s (0 for s = 0), computed on the host
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return u2f(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return u2f(w & 0xffff0000u); }
+
+// x rounded to BF16 (nearest, ties to even), as FP32.
+__device__ __forceinline__ float round_bf16(float x)
+{
+    uint16_t h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+    return u2f((uint32_t)h << 16);
+}
+
+// Last e with offs[e] <= row.
+__device__ __forceinline__ int cb_expert_of_row(const int *offs, int E, int row)
+{
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offs[mid] <= row)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+template <bool kSR>
+__global__ void __launch_bounds__(kCbThreads)
+colwise_rht_bf16_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const int32_t *__restrict__ offsets,
+                        int E, const float *__restrict__ amax_in, uint8_t *__restrict__ cw_codes,
+                        uint8_t *__restrict__ cw_scales, float *__restrict__ amax_row, float *__restrict__ amax_col,
+                        float *__restrict__ scale_enc, const __grid_constant__ PhiloxKey key, uint32_t sign_mask,
+                        uint32_t *__restrict__ status, const __grid_constant__ CbRcp rcp)
+{
+    __shared__ int offs[kCbMaxExperts + 1];
+    __shared__ float se_s[kCbMaxExperts];
+    __shared__ float rcp_s[128];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i <= E; i += kCbThreads)
+        offs[i] = __ldg(offsets + i);
+    for (int i = tid; i < 128; i += kCbThreads)
+        rcp_s[i] = rcp.v[i];
+    // per expert: amax_row = BF16_RNE(supplied amax), amax_col = 4 amax_row,
+    // S_enc = min(2688 / amax_col, FLT_MAX) (1 when amax_col = 0)
+    for (int e = tid; e < E; e += kCbThreads) {
+        const float a = round_bf16(__ldg(amax_in + e));
+        const float ac = 4.0f * a;
+        const float se = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
+        se_s[e] = se;
+        if (blockIdx.x == 0) {
+            amax_row[e] = a;
+            amax_col[e] = ac;
+            scale_enc[e] = se;
+        }
+    }
+    __syncthreads();
+    int R = offs[E];
+    if (R > R_cap) {
+        if (blockIdx.x == 0 && tid == 0)
+            raise_status(status, kDevErrCapacity);
+        R = R_cap;
+    }
+    const int ngrp = H / 16;   // 16-column groups of a row
+    const int64_t n_units = (int64_t)(R / 64) * ngrp;
+    const int j = lane & 3;    // this lane's 16-row block of the unit
+    for (int64_t wu = (int64_t)blockIdx.x * (kCbThreads / 32) + warp; wu < n_units;
+         wu += (int64_t)gridDim.x * (kCbThreads / 32)) {
+        const int rb = (int)(wu / ngrp), cg = (int)(wu % ngrp);
+        const int row0 = 64 * rb;
+        const int e = cb_expert_of_row(offs, E, row0);
+        const int off = offs[e], n = offs[e + 1] - off, rl = row0 - off;
+        if ((off & 127) != 0 || (n & 127) != 0) {
+            // an expert slot that is not whole 128-row tiles: skipped
+            if (lane == 0)
+                raise_status(status, kDevErrBadExpert);
+            continue;
+        }
+        const int P = 8 * cg + (lane >> 2);   // columns 2P and 2P + 1
+        const int h0 = 2 * P;
+        const int r0 = row0 + 16 * j;
+        uint32_t wv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            wv[i] = __ldcs(x + (int64_t)(r0 + i) * (H / 2) + P);
+        // u = sigma d / 4 (exact) and the first butterfly stage: one rounding
+        // each, fl(u_a + u_b) and fl(u_a - u_b), as FMAs of exact products
+        float2 u[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const float sa = ((sign_mask >> i) & 1u) ? -0.25f : 0.25f;
+            const float sb = ((sign_mask >> (i + 1)) & 1u) ? -0.25f : 0.25f;
+            const float2 da = mul2(make_float2(bf16_lo(wv[i]), bf16_hi(wv[i])), make_float2(sa, sa));
+            const float2 db = make_float2(bf16_lo(wv[i + 1]), bf16_hi(wv[i + 1]));
+            u[i] = __ffma2_rn(db, make_float2(sb, sb), da);
+            u[i + 1] = __ffma2_rn(db, make_float2(-sb, -sb), da);
+        }
+#pragma unroll
+        for (int len = 2; len < 16; len <<= 1) {
+#pragma unroll
+            for (int a = 0; a < 16; ++a) {
+                if (a & len)
+                    continue;
+                const float2 p = u[a], q = u[a + len];
+                u[a] = add2(p, q);
+                u[a + len] = sub2(p, q);
+            }
+        }
+        const float p0 = max3_abs(fabsf(u[0].x), u[1].x, u[2].x), q0 = max3_abs(fabsf(u[0].y), u[1].y, u[2].y);
+        const float p1 = max3_abs(fabsf(u[3].x), u[4].x, u[5].x), q1 = max3_abs(fabsf(u[3].y), u[4].y, u[5].y);
+        const float p2 = max3_abs(fabsf(u[6].x), u[7].x, u[8].x), q2 = max3_abs(fabsf(u[6].y), u[7].y, u[8].y);
+        const float p3 = max3_abs(fabsf(u[9].x), u[10].x, u[11].x), q3 = max3_abs(fabsf(u[9].y), u[10].y, u[11].y);
+        const float p4 = max3_abs(fabsf(u[12].x), u[13].x, u[14].x), q4 = max3_abs(fabsf(u[12].y), u[13].y, u[14].y);
+        const float b0 = fmaxf(fmaxf(p0, p1), max3_abs(fmaxf(p2, p3), p4, u[15].x));
+        const float b1 = fmaxf(fmaxf(q0, q1), max3_abs(fmaxf(q2, q3), q4, u[15].y));
+        const float se = se_s[e], ce = __fdiv_rn(se, 6.0f);
+        const uint32_t s2 = cvt_e4m3x2(b0 * ce, b1 * ce);
+        float2 r2;
+        const float2 sv = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(s2 & 0xffffu));
+        if (se >= 0x1p-100f && se <= 0x1p100f) {
+            // r = fl32(S_enc / s) by one Markstein step from RN(1/s); s = 0 gives 0
+            const float2 y2 = make_float2(rcp_s[s2 & 0xffu], rcp_s[(s2 >> 8) & 0xffu]);
+            const float2 se2 = make_float2(se, se);
+            const float2 qq = mul2(se2, y2);
+            const float2 ee = __ffma2_rn(make_float2(-sv.x, -sv.y), qq, se2);
+            r2 = __ffma2_rn(ee, y2, qq);
+        } else {
+            r2 = make_float2(sv.x == 0.0f ? 0.0f : __fdiv_rn(se, sv.x), sv.y == 0.0f ? 0.0f : __fdiv_rn(se, sv.y));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            u[i] = mul2(u[i], r2);
+        uint2 c0, c1;
+        if (kSR) {
+            // row i of the block takes random byte i of its column's 16 bytes (stream 2)
+            const uint64_t pos = (uint64_t)off * (uint64_t)H + (uint64_t)h0 * (uint64_t)n + (uint64_t)(rl + 16 * j);
+            const Philox4 ra = sr_bytes16(key, 2u, pos);
+            const Philox4 rb = sr_bytes16(key, 2u, pos + (uint64_t)n);
+            c0 = make_uint2(cvt_e2m1x8_sr(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x, ra.x, ra.y),
+                            cvt_e2m1x8_sr(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x,
+                                          ra.z, ra.w));
+            c1 = make_uint2(cvt_e2m1x8_sr(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y, rb.x, rb.y),
+                            cvt_e2m1x8_sr(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y,
+                                          rb.z, rb.w));
+        } else {
+            c0 = make_uint2(cvt_e2m1x8(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x),
+                            cvt_e2m1x8(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x));
+            c1 = make_uint2(cvt_e2m1x8(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y),
+                            cvt_e2m1x8(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y));
+        }
+        uint8_t *d0 = cw_codes + (int64_t)off * (H / 2) + (int64_t)h0 * (n / 2) + (rl + 16 * j) / 2;
+        *reinterpret_cast<uint2 *>(d0) = c0;
+        *reinterpret_cast<uint2 *>(d0 + n / 2) = c1;
+        // the column's 4 scale bytes of the 64 rows, gathered from its 4 lanes
+        uint32_t w0 = (s2 & 0xffu) << (8 * j), w1 = ((s2 >> 8) & 0xffu) << (8 * j);
+        w0 |= __shfl_xor_sync(0xffffffffu, w0, 1);
+        w1 |= __shfl_xor_sync(0xffffffffu, w1, 1);
+        w0 |= __shfl_xor_sync(0xffffffffu, w0, 2);
+        w1 |= __shfl_xor_sync(0xffffffffu, w1, 2);
+        if (j == 0) {
+            uint8_t *cs = cw_scales + (int64_t)off * (H / 16) + (int64_t)h0 * (n / 16) + rl / 16;
+            *reinterpret_cast<uint32_t *>(cs) = w0;
+            *reinterpret_cast<uint32_t *>(cs + n / 16) = w1;
+        }
+    }
+}
+
+static CbRcp make_cb_rcp()
+{
+    CbRcp t;
+    for (int code = 0; code < 128; ++code) {
+        const int ex = code >> 3, mt = code & 7;
+        const float v = ex == 0 ? (float)mt * (1.0f / 512.0f) : (1.0f + (float)mt / 8.0f) * ldexpf(1.0f, ex - 7);
+        t.v[code] = (v == 0.0f || code == 127) ? 0.0f : 1.0f / v;   // IEEE single division: RN(1/v)
+    }
+    return t;
+}
+
+cudaError_t launch_colwise_rht_bf16(const LaunchCtx &c, const uint16_t *x, int R_cap, int H, const int32_t *offsets,
+                                    int E, const float *amax_in, uint8_t *cw_codes, uint8_t *cw_scales,
+                                    float *amax_row, float *amax_col, float *scale_enc, int rounding, uint64_t seed,
+                                    uint32_t sign_mask, uint32_t *status)
+{
+    static const CbRcp rcp = make_cb_rcp();
+    const int64_t units = (int64_t)(R_cap / 64) * (H / 16);
+    int64_t grid = (units + (kCbThreads / 32) - 1) / (kCbThreads / 32);
+    const int64_t cap = (int64_t)c.num_sms * 4;
+    if (grid > cap)
+        grid = cap;
+    if (grid < 1)
+        grid = 1;
+    const uint32_t *xp = reinterpret_cast<const uint32_t *>(x);
+    if (rounding == 1)
+        return launch_pdl(colwise_rht_bf16_kernel<true>, dim3((unsigned)grid), dim3(kCbThreads), 0, c.stream, xp, H,
+                          R_cap, offsets, E, amax_in, cw_codes, cw_scales, amax_row, amax_col, scale_enc,
+                          philox_key(seed), sign_mask, status, rcp);
+    return launch_pdl(colwise_rht_bf16_kernel<false>, dim3((unsigned)grid), dim3(kCbThreads), 0, c.stream, xp, H,
+                      R_cap, offsets, E, amax_in, cw_codes, cw_scales, amax_row, amax_col, scale_enc,
+                      philox_key(seed), sign_mask, status, rcp);
+}
+
+} // namespace epq

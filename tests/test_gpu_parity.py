@@ -300,3 +300,74 @@ def test_route_plan_small_batch_shapes(T, E, k):
     assert_bytes_equal(plan.counts.cpu().numpy(), cnt, "counts")
     assert_bytes_equal(plan.dest.cpu().numpy()[: T * k], dest, "dest")
     assert int(plan.status.item()) == st
+
+
+def grouped_bf16_rows(w, R_cap):
+    """Expert-grouped BF16 rows [R_cap, H] of a workload (token t at each of
+    its destination rows, padding rows zero) and the exact per-expert amax."""
+    off, cnt, dest, _ = oracle.route_plan(w.topk, w.E, w.A)
+    x = np.zeros((R_cap, w.H), np.uint16)
+    d = dest.reshape(w.T, w.k)
+    for j in range(w.k):
+        ok = d[:, j] >= 0
+        x[d[ok, j]] = w.tokens[ok]
+    f = np.abs((x.astype(np.uint32) << 16).view(np.float32))
+    amax = np.zeros(w.E, np.float32)
+    for e in range(w.E):
+        if off[e + 1] > off[e]:
+            amax[e] = f[off[e]:off[e + 1]].max()
+    return x, off, amax
+
+
+@pytest.mark.parametrize("name,scale", [("cfg2", 1.0), ("cfg4", 1.0), ("cfg4_ragged_H", 1.0), ("cfg2", 3.3)])
+def test_parity_colwise_rht_bf16(name, scale):
+    """ep_nvfp4_colwise_rht_bf16 (the supplied-amax path) against the oracle,
+    byte for byte; the supplied amax is the input's own (as the dGLU epilogue
+    gives it) or larger and off the BF16 grid; rows past R are untouched."""
+    c = CASES[name]
+    w = workloads.make(c["cfg"], **c["kw"])
+    R_cap = nq.rows_capacity(w.T, w.k, w.E, w.A)
+    x, off, amax = grouped_bf16_rows(w, R_cap)
+    amax = (amax * np.float32(scale)).astype(np.float32)
+    want = oracle.nvfp4_colwise_rht_bf16(x, off, w.E, amax, rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask)
+    R, H = int(off[-1]), w.H
+    out = {"cw_codes": torch.full((R_cap * H // 2,), CANARY, dtype=torch.uint8, device="cuda"),
+           "cw_scales": torch.full((R_cap * H // 16,), CANARY, dtype=torch.uint8, device="cuda"),
+           "amax_row": torch.zeros(w.E, dtype=torch.float32, device="cuda"),
+           "amax_col": torch.zeros(w.E, dtype=torch.float32, device="cuda"),
+           "cw_scale_enc": torch.zeros(w.E, dtype=torch.float32, device="cuda")}
+    st = nq.new_status("cuda")
+    nq.ep_nvfp4_colwise_rht_bf16(to_dev_bf16(x), torch.from_numpy(off).cuda(), w.E, torch.from_numpy(amax).cuda(),
+                                 out=out, rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    g = {k: v.cpu().numpy() for k, v in out.items()}
+    assert_bytes_equal(g["cw_codes"][: R * H // 2], want["cw_codes"][: R * H // 2], "columnwise codes")
+    assert_bytes_equal(g["cw_scales"][: R * H // 16], want["cw_scales"][: R * H // 16], "columnwise scales")
+    assert (g["cw_codes"][R * H // 2:] == CANARY).all() and (g["cw_scales"][R * H // 16:] == CANARY).all()
+    for k, ok in (("amax_row", "amax_row"), ("amax_col", "amax_col"), ("cw_scale_enc", "scale_enc")):
+        assert_bytes_equal(g[k].view(np.uint32), want[ok].view(np.uint32), k)
+    assert want["report"]["above_4x_rowwise_amax"] == 0
+
+
+def test_colwise_rht_bf16_rejects_partial_slots():
+    """Expert slots that are not whole 128-row tiles: the device status says
+    so and their rows are skipped (the other experts are still written)."""
+    H, E = 64, 2
+    off = np.array([0, 128, 200], np.int32)          # expert 1: 72 rows
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((256, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    amax = np.array([4.0, 4.0], np.float32)
+    out = {"cw_codes": torch.full((256 * H // 2,), CANARY, dtype=torch.uint8, device="cuda"),
+           "cw_scales": torch.full((256 * H // 16,), CANARY, dtype=torch.uint8, device="cuda"),
+           "amax_row": torch.zeros(E, dtype=torch.float32, device="cuda"),
+           "amax_col": torch.zeros(E, dtype=torch.float32, device="cuda"),
+           "cw_scale_enc": torch.zeros(E, dtype=torch.float32, device="cuda")}
+    st = nq.new_status("cuda")
+    nq.ep_nvfp4_colwise_rht_bf16(to_dev_bf16(x), torch.from_numpy(off).cuda(), E, torch.from_numpy(amax).cuda(),
+                                 out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & nq.EP_DEV_ERR_BAD_EXPERT
+    want = oracle.nvfp4_colwise_rht_bf16(x[:128], np.array([0, 128], np.int32), 1, amax[:1])
+    assert_bytes_equal(out["cw_codes"].cpu().numpy()[: 128 * H // 2], want["cw_codes"], "expert 0 codes")
+    assert (out["cw_codes"].cpu().numpy()[128 * H // 2:] == CANARY).all()
