@@ -87,6 +87,7 @@ def _declare(L):
     L.or_scale_swizzle.argtypes = [_P, _I64, _I64, _P]; L.or_scale_swizzle.restype = None
     L.or_nvfp4_colwise_rht_bf16.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _P, _I32, _U64, _U16, _P]
     L.or_nvfp4_colwise_rht_bf16.restype = None
+    L.or_mxfp8_colwise.argtypes = [_P, _I64, _I64, _P, _I32, _P]; L.or_mxfp8_colwise.restype = None
     L.or_nvfp4_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _I32, _U64]
     L.or_nvfp4_pack.restype = None
     L.or_nvfp4_unpack.argtypes = [_P, _I64, _I64, _P, _I32, _P]
@@ -339,6 +340,18 @@ def nvfp4_colwise_rht_bf16(x_bf16: np.ndarray, offsets, E, amax_in, rounding: in
     out["report"] = dict(scale_saturated=int(report[0]), above_4x_rowwise_amax=int(report[1]),
                          element_saturated=int(report[2]), above_4x_block_input=int(report[3]))
     return out
+
+
+def mxfp8_colwise(x_bf16: np.ndarray, offsets, E) -> np.ndarray:
+    """Expert-grouped BF16 rows [R_cap, H] -> one buffer: the columnwise MXFP8
+    data (expert e: [H][n_e] at offsets[e]*H) then scales (expert e:
+    [H][n_e/32] at R_cap*H + offsets[e]*H/32) (reading R25)."""
+    x = _as(x_bf16, np.uint16)
+    R_cap, H = x.shape
+    offsets = _as(offsets, np.int32)
+    buf = np.zeros(R_cap * H + R_cap * (H // 32), np.uint8)
+    lib().or_mxfp8_colwise(_ptr(x), R_cap, H, _ptr(offsets), E, _ptr(buf))
+    return buf
 
 
 def mxfp8_pack(tokens_bf16: np.ndarray, dest, k, offsets, counts, E, R_cap) -> np.ndarray:

@@ -103,6 +103,9 @@ void     or_nvfp4_colwise_rht_bf16(const uint16_t *x, int64_t R_cap, int64_t H,
                                    float *amax_col, float *scale_enc,
                                    int rounding, uint64_t seed,
                                    uint16_t sign_mask, int64_t *report);
+/* Columnwise MXFP8 operand of an expert-grouped BF16 tensor (R25). */
+void     or_mxfp8_colwise(const uint16_t *x, int64_t R_cap, int64_t H,
+                          const int32_t *offsets, int E, uint8_t *buf);
 /* Tiled scale-factor layout (R23): M % 128 == 0, Kb % 4 == 0. */
 void     or_scale_swizzle(const uint8_t *lin, int64_t M, int64_t Kb, uint8_t *out);
 void     or_mxfp8_pack(const uint16_t *tokens, int64_t T, int64_t H,
