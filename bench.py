@@ -377,6 +377,11 @@ def aux_measure(torch, nq, w, b, R, reps=20):
                                                       status=b.plan.status))
     res["colwise_rht_bf16"] = {"ms": ms_c, "bytes": R * H * 2 + R * (9 * H // 16) + 16 * w.E}
     del cw
+    # the columnwise MXFP8 operand of the same BF16 rows
+    mxc = torch.empty(b.plan.R_cap * H + b.plan.R_cap * (H // 32), dtype=torch.uint8, device="cuda")
+    ms_x = timed(lambda: nq.ep_mxfp8_colwise(out, b.plan.offsets, w.E, buf=mxc, status=b.plan.status))
+    res["mxfp8_colwise"] = {"ms": ms_x, "bytes": R * H * 2 + R * (H + H // 32)}
+    del mxc
     if H % 128 == 0:
         g = nq.alloc_grouped(b.plan.R_cap, H, w.E, "cuda")
         bytes_d = algorithmic_bytes(w.T, H, w.k, w.E, R, S)[2]

@@ -337,6 +337,29 @@ ep_status ep_mxfp8_pack(const void *tokens_bf16, int64_t T, int64_t H,
                         const int32_t *expert_counts, int E, uint8_t *buf,
                         int64_t R_cap, uint32_t *dev_status, void *stream);
 
+/*
+ * ep_mxfp8_colwise -- the columnwise (weight-gradient) MXFP8 operand of an
+ * expert-grouped BF16 tensor: 32-element blocks along the token axis.
+ * TE PR #3270, Description: the combine backward returns the expert-output
+ * gradient as a per-expert MXFP8 GroupedTensor; Changes: data and block
+ * scales in one caller-supplied buffer, data first.
+ *   x_bf16          device bf16 [R_cap, H], rows in expert order (expert e:
+ *                   rows [expert_offsets[e], expert_offsets[e+1]), whole
+ *                   128-row tiles, else EP_DEV_ERR_BAD_EXPERT and the expert
+ *                   is skipped).  Finite values.
+ *   buf             device u8: data, expert e as [H][n_e] bytes at byte
+ *                   expert_offsets[e]*H (column h's rows along the bytes);
+ *                   then, from byte R_cap*H, scales, expert e as [H][n_e/32]
+ *                   at expert_offsets[e]*H/32.  Bytes of rows past R are left
+ *                   untouched.
+ * Per column and 32-row block: e = smallest integer in [-127, 127] with
+ * max|x| <= 448*2^e, scale byte e + 127, element E4M3_RNE(x / 2^e) (as
+ * ep_mxfp8_pack along the other axis).
+ */
+ep_status ep_mxfp8_colwise(const void *x_bf16, int64_t R_cap, int64_t H,
+                           const int32_t *expert_offsets, int E, uint8_t *buf,
+                           uint32_t *dev_status, void *stream);
+
 /* Human-readable name of a status code. */
 const char *ep_status_string(int status);
 

@@ -28,7 +28,8 @@ EP_ROUTE_STATIC_SCRATCH_BYTES = 262144   # mirrors the macro in include/epq.h
 # every symbol include/epq.h declares
 SYMBOLS = ("ep_nvfp4_row_bytes", "ep_rows_capacity", "ep_route_workspace_bytes", "ep_route_plan",
            "ep_route_plan_noalloc", "ep_nvfp4_pack", "ep_nvfp4_dispatch", "ep_nvfp4_unpack", "ep_nvfp4_direct_receive",
-           "ep_nvfp4_direct_receive_swizzled", "ep_nvfp4_colwise_rht_bf16", "ep_mxfp8_pack", "ep_status_string")
+           "ep_nvfp4_direct_receive_swizzled", "ep_nvfp4_colwise_rht_bf16", "ep_mxfp8_pack",
+           "ep_mxfp8_colwise", "ep_status_string")
 
 
 class EpGrouped(ctypes.Structure):
@@ -70,6 +71,8 @@ def _declare(L):
     L.ep_nvfp4_colwise_rht_bf16.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _P, _I32, _U64,
                                             ctypes.c_uint16, _P, _P]
     L.ep_nvfp4_colwise_rht_bf16.restype = _I32
+    L.ep_mxfp8_colwise.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _P]
+    L.ep_mxfp8_colwise.restype = _I32
     L.ep_mxfp8_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _P, _P]
     L.ep_mxfp8_pack.restype = _I32
     L.ep_status_string.argtypes = [_I32]; L.ep_status_string.restype = ctypes.c_char_p

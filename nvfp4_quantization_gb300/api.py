@@ -243,6 +243,21 @@ def ep_nvfp4_colwise_rht_bf16(x: torch.Tensor, offsets: torch.Tensor, E: int, am
     return out
 
 
+def ep_mxfp8_colwise(x: torch.Tensor, offsets: torch.Tensor, E: int, buf: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Expert-grouped BF16 rows [R_cap, H] -> one uint8 buffer: the columnwise
+    MXFP8 data (expert e: [H][n_e]) then scales (expert e: [H][n_e/32])."""
+    _need_cuda(x, "x", torch.bfloat16)
+    R_cap, H = x.shape
+    if buf is None:
+        buf = torch.empty(R_cap * H + R_cap * (H // 32), dtype=torch.uint8, device=x.device)
+    if status is None:
+        status = new_status(x.device)
+    st = _lib.lib().ep_mxfp8_colwise(_ptr(x), R_cap, H, _ptr(offsets), E, _ptr(buf), _ptr(status), _stream(stream))
+    check("ep_mxfp8_colwise", st)
+    return buf
+
+
 def ep_mxfp8_pack(tokens: torch.Tensor, plan: RoutePlan, buf: torch.Tensor | None = None,
                   stream=None) -> torch.Tensor:
     """BF16 tokens -> one uint8 buffer: data [R_cap, H] then scales [R_cap, H/32]."""

@@ -242,6 +242,28 @@ ep_status ep_nvfp4_colwise_rht_bf16(const void *x_bf16, int64_t R_cap, int64_t H
                                                     cw_scale_enc, rounding, seed, rht_sign_mask, dev_status));
 }
 
+ep_status ep_mxfp8_colwise(const void *x_bf16, int64_t R_cap, int64_t H, const int32_t *expert_offsets, int E,
+                           uint8_t *buf, uint32_t *dev_status, void *stream)
+{
+    if (!x_bf16 || !expert_offsets || !buf || !dev_status)
+        return EP_ERR_NULL;
+    if (!shape_ok(0, H, 1, E))
+        return EP_ERR_SHAPE;
+    if (R_cap < 0 || R_cap > (int64_t)INT32_MAX || R_cap * H > (int64_t)INT32_MAX * 32)
+        return EP_ERR_CAPACITY;
+    if (!aligned16(x_bf16) || !aligned16(buf))
+        return EP_ERR_ALIGN;
+    const int dev = device_of(x_bf16);
+    if (dev < 0 || !on_device(expert_offsets, dev) || !on_device(buf, dev) || !on_device(dev_status, dev))
+        return EP_ERR_DEVICE;
+    DeviceGuard g(dev);
+    if (!g.ok)
+        return EP_ERR_DEVICE;
+    LaunchCtx c{(cudaStream_t)stream, dev, sm_count(dev)};
+    return cuda_status(epq::launch_mxfp8_colwise(c, (const uint16_t *)x_bf16, (int)R_cap, (int)H, expert_offsets, E,
+                                                 buf, dev_status));
+}
+
 ep_status ep_mxfp8_pack(const void *tokens_bf16, int64_t T, int64_t H, const int32_t *dest, int k,
                         const int32_t *expert_offsets, const int32_t *expert_counts, int E, uint8_t *buf,
                         int64_t R_cap, uint32_t *dev_status, void *stream)

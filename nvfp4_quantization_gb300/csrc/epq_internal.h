@@ -89,6 +89,9 @@ cudaError_t launch_colwise_rht_bf16(const LaunchCtx &c, const uint16_t *x, int R
                                     float *amax_row, float *amax_col, float *scale_enc, int rounding, uint64_t seed,
                                     uint32_t sign_mask, uint32_t *status);
 
+cudaError_t launch_mxfp8_colwise(const LaunchCtx &c, const uint16_t *x, int R_cap, int H, const int32_t *offsets,
+                                 int E, uint8_t *buf, uint32_t *status);
+
 // swz: both scale tensors in the tiled layout of block-scaled GEMM operands
 // (H % 128 == 0, checked by the caller).
 cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,

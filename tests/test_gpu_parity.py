@@ -371,3 +371,26 @@ def test_colwise_rht_bf16_rejects_partial_slots():
     want = oracle.nvfp4_colwise_rht_bf16(x[:128], np.array([0, 128], np.int32), 1, amax[:1])
     assert_bytes_equal(out["cw_codes"].cpu().numpy()[: 128 * H // 2], want["cw_codes"], "expert 0 codes")
     assert (out["cw_codes"].cpu().numpy()[128 * H // 2:] == CANARY).all()
+
+
+@pytest.mark.parametrize("name", ["cfg5", "cfg1_ragged_H", "cfg4"])
+def test_parity_mxfp8_colwise(name):
+    """ep_mxfp8_colwise against the oracle, byte for byte (data and scales of
+    rows [0, R)); bytes of rows past R untouched.  The ragged case has H % 64
+    = 32 (a half-filled last column group)."""
+    c = CASES[name]
+    w = workloads.make(c["cfg"], **c["kw"])
+    R_cap = nq.rows_capacity(w.T, w.k, w.E, w.A)
+    x, off, _ = grouped_bf16_rows(w, R_cap)
+    want = oracle.mxfp8_colwise(x, off, w.E)
+    buf = torch.full((R_cap * w.H + R_cap * (w.H // 32),), CANARY, dtype=torch.uint8, device="cuda")
+    st = nq.new_status("cuda")
+    nq.ep_mxfp8_colwise(to_dev_bf16(x), torch.from_numpy(off).cuda(), w.E, buf=buf, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = buf.cpu().numpy()
+    R, H = int(off[-1]), w.H
+    assert_bytes_equal(got[: R * H], want[: R * H], "mxfp8 columnwise data")
+    assert_bytes_equal(got[R_cap * H: R_cap * H + R * H // 32], want[R_cap * H: R_cap * H + R * H // 32],
+                       "mxfp8 columnwise scales")
+    assert (got[R * H: R_cap * H] == CANARY).all() and (got[R_cap * H + R * H // 32:] == CANARY).all()
