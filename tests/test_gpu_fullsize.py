@@ -164,3 +164,66 @@ def test_mxfp8_sampled_tokens(run):
     for d in sub_dest[sub_dest >= 0]:
         assert_bytes_equal(gd[d], wd[d], f"mxfp8 data row {d}")
         assert_bytes_equal(gs[d], ws[d], f"mxfp8 scale row {d}")
+
+
+def test_swizzled_scales_of_sampled_experts(run):
+    """The swizzled call on the full batch: for the two sampled experts, the
+    columnwise scales equal the oracle's scales in the tiled layout, and the
+    rowwise tiles of their rows equal the tiled rowwise scales."""
+    w = run.w
+    H = w.H
+    if H % 128:
+        pytest.skip("the tiled layout needs H % 128 == 0")
+    g = nq.ep_nvfp4_direct_receive(run.rows, H, run.plan.offsets, w.E, rounding=w.rounding, seed=w.seed,
+                                   sign_mask=w.sign_mask, status=run.plan.status, swizzled=True)
+    lin = run.out
+    torch.cuda.synchronize()
+    for e in sampled_experts(run):
+        a, b = int(run.off[e]), int(run.off[e + 1])
+        n = b - a
+        want_cw = oracle.scale_swizzle(lin["cw_scales"][a * H // 16:b * H // 16].cpu().numpy().reshape(H, n // 16))
+        assert_bytes_equal(g["cw_scales"][a * H // 16:b * H // 16].cpu().numpy(), want_cw,
+                           f"tiled columnwise scales of expert {e}")
+        want_rw = oracle.scale_swizzle(lin["rw_scales"][a:b].cpu().numpy())
+        assert_bytes_equal(g["rw_scales"].reshape(-1)[a * H // 16:b * H // 16].cpu().numpy(), want_rw,
+                           f"tiled rowwise scales of expert {e}")
+        assert torch.equal(g["cw_codes"][a * H // 2:b * H // 2], lin["cw_codes"][a * H // 2:b * H // 2])
+
+
+def test_bf16_columnwise_paths_of_sampled_experts(run):
+    """The BF16-input columnwise calls on the full batch's decoded rows (the
+    unpack of the received rows, as the bench times them), checked for the
+    sampled experts against the oracle run on those experts' rows alone:
+    the supplied-amax RHT quantizer (given the direct receive's amaxes) and
+    the columnwise MXFP8 operand."""
+    w = run.w
+    H = w.H
+    x = nq.ep_nvfp4_unpack(run.rows, H, run.plan.offsets, w.E, status=run.plan.status)
+    amax = run.out["amax_row"]
+    cw = nq.ep_nvfp4_colwise_rht_bf16(x, run.plan.offsets, w.E, amax, rounding=w.rounding, seed=w.seed,
+                                      sign_mask=w.sign_mask, status=run.plan.status)
+    mx = nq.ep_mxfp8_colwise(x, run.plan.offsets, w.E, status=run.plan.status)
+    torch.cuda.synchronize()
+    assert int(run.plan.status.item()) == 0
+    R_cap = run.R_cap
+    am = amax.cpu().numpy()
+    for e in sampled_experts(run):
+        a, b = int(run.off[e]), int(run.off[e + 1])
+        n = b - a
+        xe = x[a:b].view(torch.int16).cpu().numpy().view(np.uint16)
+        # the oracle on this expert alone: its rows at offset 0
+        o = oracle.nvfp4_colwise_rht_bf16(xe, np.array([0, n], np.int32), 1, am[e:e + 1], rounding=w.rounding,
+                                          seed=w.seed, sign_mask=w.sign_mask)
+        # SR keys on the element's index off*H + h*n + row: the oracle's off is 0, so
+        # compare codes only for RNE; scales and metadata for both
+        if w.rounding == 0:
+            assert_bytes_equal(cw["cw_codes"][a * H // 2:b * H // 2].cpu().numpy(), o["cw_codes"],
+                               f"supplied-amax codes of expert {e}")
+        assert_bytes_equal(cw["cw_scales"][a * H // 16:b * H // 16].cpu().numpy(), o["cw_scales"],
+                           f"supplied-amax scales of expert {e}")
+        assert cw["cw_scale_enc"][e].item() == o["scale_enc"][0]
+        om = oracle.mxfp8_colwise(xe, np.array([0, n], np.int32), 1)
+        got = mx.cpu().numpy()
+        assert_bytes_equal(got[a * H:b * H], om[: n * H], f"columnwise MXFP8 data of expert {e}")
+        assert_bytes_equal(got[R_cap * H + a * H // 32:R_cap * H + b * H // 32], om[n * H:],
+                           f"columnwise MXFP8 scales of expert {e}")
