@@ -394,3 +394,29 @@ def test_parity_mxfp8_colwise(name):
     assert_bytes_equal(got[R_cap * H: R_cap * H + R * H // 32], want[R_cap * H: R_cap * H + R * H // 32],
                        "mxfp8 columnwise scales")
     assert (got[R * H: R_cap * H] == CANARY).all() and (got[R_cap * H + R * H // 32:] == CANARY).all()
+
+
+def test_route_barrier_timeout_is_reported():
+    """Failure detection without a fault: the routing plan's grid barrier is
+    given an arrival count preset far beyond the grid (so no CTA can be the
+    last to arrive: a flag nothing sets).  Its bounded wait gives up, the
+    kernel returns with EP_DEV_ERR_TIMEOUT in the device status, and the
+    context stays usable: the next plan (fresh workspace) is exact."""
+    import time
+    T, E, k = 3000, 32, 12          # k > 8: the cooperative kernel with the grid barrier
+    rng = np.random.default_rng(21)
+    topk = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    tk = torch.from_numpy(topk).cuda()
+    ws = nq.new_route_workspace(T, k, E, "cuda")
+    ws[0] = 0x40000000
+    t0 = time.perf_counter()
+    plan = nq.ep_route_plan(tk, E, 128, workspace=ws)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(plan.status.item()) & nq.EP_DEV_ERR_TIMEOUT
+    assert waited < 30.0
+    good = nq.ep_route_plan(tk, E, 128)
+    torch.cuda.synchronize()
+    off, cnt, dest, st = oracle.route_plan(topk, E, 128)
+    assert int(good.status.item()) == st == 0
+    assert_bytes_equal(good.dest.cpu().numpy()[: T * k], dest, "dest after a timed-out plan")
