@@ -420,3 +420,22 @@ def test_route_barrier_timeout_is_reported():
     off, cnt, dest, st = oracle.route_plan(topk, E, 128)
     assert int(good.status.item()) == st == 0
     assert_bytes_equal(good.dest.cpu().numpy()[: T * k], dest, "dest after a timed-out plan")
+
+
+def test_parity_largest_expert_count_and_slots():
+    """E = 1024 experts (the largest allowed) and k = 32 slots per token:
+    the general routing kernel, 1 024 mostly-padding slots, the direct
+    receive's per-CTA expert tables at their full size."""
+    w = workloads.make(4, T=64, H=256, E=1024, k=32)
+    g = GpuRun(w)
+    o = OracleRun(w, g.R_cap)
+    compare_runs(g, o)
+
+
+def test_parity_wide_hidden():
+    """H = 16384: the pack's multi-chunk kernel (wider than the warp kernel's
+    8192) and 64 column strips in the direct receive."""
+    w = workloads.make(1, T=64, H=16384)
+    g = GpuRun(w, unpack=True, mxfp8=True)
+    o = OracleRun(w, g.R_cap, unpack=True, mxfp8=True)
+    compare_runs(g, o)
