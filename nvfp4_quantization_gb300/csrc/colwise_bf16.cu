@@ -96,8 +96,29 @@ colwise_rht_bf16_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const 
     const int ngrp = H / 16;   // 16-column groups of a row
     const int64_t n_units = (int64_t)(R / 64) * ngrp;
     const int j = lane & 3;    // this lane's 16-row block of the unit
-    for (int64_t wu = (int64_t)blockIdx.x * (kCbThreads / 32) + warp; wu < n_units;
-         wu += (int64_t)gridDim.x * (kCbThreads / 32)) {
+    const int64_t stride = (int64_t)gridDim.x * (kCbThreads / 32);
+    // the next unit's 16 words are requested before this unit's arithmetic
+    // (its loads do not depend on the expert), so a warp keeps its loads in
+    // flight while it computes
+    auto load_unit = [&](int64_t u, uint32_t(&w)[16]) {
+        const int rb = (int)(u / ngrp), cg = (int)(u % ngrp);
+        const int P = 8 * cg + (lane >> 2);
+        const int64_t r0 = 64 * (int64_t)rb + 16 * j;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = __ldcs(x + (r0 + i) * (H / 2) + P);
+    };
+    int64_t wu = (int64_t)blockIdx.x * (kCbThreads / 32) + warp;
+    uint32_t wv[16];
+    if (wu < n_units)
+        load_unit(wu, wv);
+    for (; wu < n_units; wu += stride) {
+        uint32_t wcur[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            wcur[i] = wv[i];
+        if (wu + stride < n_units)
+            load_unit(wu + stride, wv);
         const int rb = (int)(wu / ngrp), cg = (int)(wu % ngrp);
         const int row0 = 64 * rb;
         const int e = cb_expert_of_row(offs, E, row0);
@@ -110,11 +131,6 @@ colwise_rht_bf16_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const 
         }
         const int P = 8 * cg + (lane >> 2);   // columns 2P and 2P + 1
         const int h0 = 2 * P;
-        const int r0 = row0 + 16 * j;
-        uint32_t wv[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            wv[i] = __ldcs(x + (int64_t)(r0 + i) * (H / 2) + P);
         // u = sigma d / 4 (exact) and the first butterfly stage: one rounding
         // each, fl(u_a + u_b) and fl(u_a - u_b), as FMAs of exact products
         float2 u[16];
@@ -122,8 +138,8 @@ colwise_rht_bf16_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const 
         for (int i = 0; i < 16; i += 2) {
             const float sa = ((sign_mask >> i) & 1u) ? -0.25f : 0.25f;
             const float sb = ((sign_mask >> (i + 1)) & 1u) ? -0.25f : 0.25f;
-            const float2 da = mul2(make_float2(bf16_lo(wv[i]), bf16_hi(wv[i])), make_float2(sa, sa));
-            const float2 db = make_float2(bf16_lo(wv[i + 1]), bf16_hi(wv[i + 1]));
+            const float2 da = mul2(make_float2(bf16_lo(wcur[i]), bf16_hi(wcur[i])), make_float2(sa, sa));
+            const float2 db = make_float2(bf16_lo(wcur[i + 1]), bf16_hi(wcur[i + 1]));
             u[i] = __ffma2_rn(db, make_float2(sb, sb), da);
             u[i + 1] = __ffma2_rn(db, make_float2(-sb, -sb), da);
         }
