@@ -49,14 +49,17 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int sm_count(int dev)
 {
-    static int cache[64] = {0};
-    if (dev >= 0 && dev < 64 && cache[dev] > 0)
-        return cache[dev];
+    static std::atomic<int> cache[64] = {};
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0)
+            return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         n = 1;
     if (dev >= 0 && dev < 64)
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

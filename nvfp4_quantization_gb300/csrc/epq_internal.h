@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace epq {
@@ -39,15 +40,18 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Sets the dynamic shared-memory limit of `kernel` once per device (it is a
 // per-function attribute; setting it again inside a stream capture is avoided).
+// The per-device flags are atomic: calls from several host threads may race to
+// set the same attribute, which is harmless.
 template <typename K>
-cudaError_t ensure_smem_limit(K kernel, int device, int bytes, int *done_mask_words /*[2]*/)
+cudaError_t ensure_smem_limit(K kernel, int device, int bytes, std::atomic<uint32_t> *done_mask_words /*[2]*/)
 {
-    const int w = device >> 5, b = device & 31;
-    if (device >= 0 && device < 64 && (done_mask_words[w] >> b) & 1)
+    const int w = device >> 5;
+    const uint32_t bit = 1u << (device & 31);
+    if (device >= 0 && device < 64 && (done_mask_words[w].load(std::memory_order_acquire) & bit))
         return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && device >= 0 && device < 64)
-        done_mask_words[w] |= (1 << b);
+        done_mask_words[w].fetch_or(bit, std::memory_order_release);
     return e;
 }
 

@@ -681,7 +681,7 @@ static cudaError_t launch_nvfp4_warp(const LaunchCtx &c, const uint16_t *tokens,
     const int64_t S = row_bytes(H);
     const int th = 32 * kPackWarps, wpb = kPackWarps;
     const size_t smem = (size_t)kPackWarps * kBuf * 2 * (size_t)H;
-    static int done_rn[2] = {0, 0}, done_sr[2] = {0, 0};
+    static std::atomic<uint32_t> done_rn[2] = {}, done_sr[2] = {};
     cudaError_t err = rounding == 1 ? ensure_smem_limit(nvfp4_pack_warp_kernel<NB, true>, c.device, (int)smem, done_sr)
                                     : ensure_smem_limit(nvfp4_pack_warp_kernel<NB, false>, c.device, (int)smem, done_rn);
     if (err != cudaSuccess)

@@ -770,7 +770,7 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
 
     const bool sr = rounding == 1;
     const size_t smem = (sr ? sizeof(DrCfg<true>::Smem) : sizeof(DrCfg<false>::Smem)) + 1024;
-    static int done[4][2] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}};
+    static std::atomic<uint32_t> done[4][2] = {};
     auto kern = sr ? (swz ? direct_receive_kernel<true, true> : direct_receive_kernel<true, false>)
                    : (swz ? direct_receive_kernel<false, true> : direct_receive_kernel<false, false>);
     err = ensure_smem_limit(kern, c.device, (int)smem, done[(sr ? 2 : 0) + (swz ? 1 : 0)]);

@@ -417,7 +417,7 @@ cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, in
                               uint32_t *status)
 {
     const size_t smem = (size_t)E * kWords * 4u * 2u + (size_t)E * 4u * 4u;
-    static int done[2] = {0, 0}, done_reg[2] = {0, 0}, done_cl[2] = {0, 0};
+    static std::atomic<uint32_t> done[2] = {}, done_reg[2] = {}, done_cl[2] = {};
     cudaError_t err = ensure_smem_limit(route_plan_kernel, c.device, 1024 * kWords * 8 + 1024 * 16, done);
     if (err == cudaSuccess)
         err = ensure_smem_limit(route_plan_reg_kernel<false>, c.device, 1024 * kWords * 8 + 1024 * 16, done_reg);
