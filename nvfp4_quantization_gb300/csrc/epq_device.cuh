@@ -328,6 +328,14 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(const void *p, uint32_t rank)
     return v;
 }
 
+// Packed f16 product, round to nearest even.
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // max(m, |a|, |b|) in one three-input maximum (finite inputs).
 __device__ __forceinline__ float max3_abs(float m, float a, float b)
 {

@@ -442,7 +442,18 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
                 float f = w4 != 0u ? exp2i(k - K - 2) : 0.0f;
                 if (neg)
                     f = -f;
-                const uint32_t lo = cvt_f16x2(a.x * f, a.y * f), hi = cvt_f16x2(b.x * f, b.y * f);
+                uint32_t lo, hi;
+                if (kSR) {
+                    // the same exact values as f16 products of exact f16
+                    // values (2^(k-K-2) in 2^[-15, -2], subnormal at -15):
+                    // fewer registers live in the SR kernel
+                    const uint32_t f2 = cvt_f16x2(f, f);
+                    lo = hmul2_rn(cvt_f16x2_from_e4m3x2(w4 & 0xffffu), f2);
+                    hi = hmul2_rn(cvt_f16x2_from_e4m3x2(w4 >> 16), f2);
+                } else {
+                    lo = cvt_f16x2(a.x * f, a.y * f);
+                    hi = cvt_f16x2(b.x * f, b.y * f);
+                }
                 t16[0][rloc] = (uint16_t)lo;
                 t16[1][rloc] = (uint16_t)(lo >> 16);
                 t16[2][rloc] = (uint16_t)hi;
