@@ -441,7 +441,28 @@ def e2e_measure(torch, nq, w, bufs, tok_host, topk_host, R, steps):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     ok = all(torch.equal(dsts[3][: 1 << 16].cuda(), srcs[3][: 1 << 16]) for _, _, srcs, dsts in lanes)
-    return dict(ms=ms, h2d=h2d, d2h=d2h, ok=bool(ok))
+    return dict(ms=ms, h2d=h2d, d2h=d2h, ok=bool(ok), link=host_link_gbs(torch))
+
+
+def host_link_gbs(torch, nbytes: int = 256 << 20, reps: int = 5) -> dict:
+    """Plain pinned-memory copy bandwidth of this GPU's host link in each
+    direction (one copy at a time): the floor of the end-to-end step is its
+    bytes over these rates."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        out[name] = reps * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+    return out
 
 
 def oracle_pass(o, w, tokens, topk):
@@ -548,7 +569,11 @@ def main():
         "e2e": {"value": world * r["T"] / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"],
                 "api": "eager ep_nvfp4_dispatch / ep_nvfp4_direct_receive on two streams, "
-                       "alternate steps (double buffering)", "checked": e2e["ok"]},
+                       "alternate steps (double buffering)", "checked": e2e["ok"],
+                "host_link_gbs": e2e["link"],
+                "link_floor_ms": max(e2e["h2d"] / (e2e["link"]["h2d"] * 1e9), e2e["d2h"] / (e2e["link"]["d2h"] * 1e9)) * 1e3,
+                "floor_note": "the larger of the step's host-to-device and device-to-host bytes over the pinned "
+                              "copy bandwidth of that direction (copies in the two directions overlap)"},
         "other_calls": {name: {"ms": v["ms"], "gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9,
                                "frac": v["bytes"] / (v["ms"] * 1e-3) / 1e9 / peak, "bytes": v["bytes"],
                                "note": "one call on the step's batch, L2 flushed before each launch"}
