@@ -153,9 +153,9 @@ ep_status ep_route_plan_noalloc(const int32_t *topk_idx, int64_t T, int k,
  * ep_nvfp4_pack -- quantise each BF16 token once into a packed NVFP4 row and
  * write that row to each of its destinations; fill padding rows.
  * TE PR #3753, PR description and the review thread on the EP header comment:
- * "the sender packs each token into one NVFP4 row (E2M1 codes, E4M3 block
- * scales and a power-of-two FP32 token scale)"; the combine backward "uses
- * stochastic rounding per the recipe".
+ * each token is quantised a single time on the sending side, into a row of
+ * E2M1 codes with E4M3 scales per 16 elements and an FP32 token scale that is
+ * a power of two; the combine backward takes the recipe's stochastic rounding.
  *   tokens_bf16     device bf16 [T, H] row-major, finite values.
  *   dest, expert_offsets, expert_counts: as produced by ep_route_plan.
  *   rows            device u8 [R_cap, S], S = ep_nvfp4_row_bytes(H), 16-byte
@@ -205,9 +205,9 @@ ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16,
 
 /*
  * ep_nvfp4_unpack -- decode packed rows to BF16 (the path used when direct
- * receive is off).  TE PR #3753, PR description: "Otherwise the rows are
- * decoded to BF16"; commit "grad direct-receive opt-out": the opt-out returns
- * the BF16 decode of the received rows.
+ * receive is off).  TE PR #3753, PR description: without direct receive the
+ * received rows are turned back into BF16; commit "grad direct-receive
+ * opt-out": the opt-out returns that BF16 decode.
  *   rows            device u8 [R_cap, S] (ep_nvfp4_pack layout).
  *   out_bf16        device bf16 [R_cap, H]; rows [0, R) written with
  *                   BF16(sign * E2M1 value * s_b * S_t) (exact in BF16 except
@@ -235,11 +235,12 @@ typedef struct {
 /*
  * ep_nvfp4_direct_receive -- build the expert GEMM's grouped NVFP4 operands
  * straight from the packed rows, in one pass over them.
- * TE PR #3753, PR description: "the rowwise operand reuses the sender's codes
- * and the columnwise RHT operand is quantized with a bound-derived per-expert
- * scale, so no BF16 round trip or amax pass is needed"; TE PR #3755, PR
- * description: "the post-RHT columnwise amax is bounded by 4x the rowwise
- * amax"; TE PR #3324, description: row-scaled (per-token) NVFP4 operands.
+ * TE PR #3753, PR description: the rowwise operand keeps the codes the sender
+ * produced, and the columnwise RHT operand is requantised with a per-expert
+ * scale derived from a bound, which avoids both a trip through BF16 and a pass
+ * that measures the amax; TE PR #3755, PR description: after the RHT no
+ * columnwise value exceeds four times the rowwise amax; TE PR #3324,
+ * description: NVFP4 operands with one FP32 scale per row (per token).
  *   rows            device u8 [R_cap, S].
  *   out             host pointer to the output descriptor.  The rowwise group
  *                   (rw_codes, rw_scales, rw_row_scale) may be all NULL to skip
@@ -265,9 +266,9 @@ ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
 /*
  * ep_nvfp4_direct_receive_swizzled -- ep_nvfp4_direct_receive with both scale
  * tensors in the tiled layout that block-scaled GEMMs read.
- * TE PR #3753, commit "... under NVFP4 autocast": the combine backward returns
- * FC2's gradient as a "swizzled NVFP4 GroupedTensor" holding only GEMM
- * operands.  The pages do not spell the layout out; the one used is the
+ * TE PR #3753, commit "... under NVFP4 autocast": the combine backward hands
+ * FC2's gradient over as a grouped NVFP4 tensor whose scales are already in
+ * the GEMM's swizzled order and which carries GEMM operands only.  The pages do not spell the layout out; the one used is the
  * Blackwell block-scaled operand layout: a scale matrix SF[M][Kb] is cut into
  * 512-byte tiles of 128 rows x 4 scale columns, tile (mt, kt) at byte
  * (mt*Kb/4 + kt)*512, and element (m, kb) of a tile at
@@ -292,9 +293,9 @@ ep_status ep_nvfp4_direct_receive_swizzled(const uint8_t *rows, int64_t R_cap,
  * ep_nvfp4_colwise_rht_bf16 -- the columnwise RHT operand of an expert-grouped
  * BF16 tensor, with the per-expert amax supplied by its producer.
  * TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the dGLU epilogue",
- * PR description: "the rowwise amax is the exact dGLU epilogue amax rounded
- * to BF16; the post-RHT columnwise amax is bounded by 4x the rowwise amax;
- * skips the separate grouped amax pass".
+ * PR description: the dGLU epilogue's exact amax, rounded to BF16, serves as
+ * the rowwise amax; four times it bounds the columnwise amax after the RHT, so
+ * the grouped tensor needs no amax pass of its own.
  *   x_bf16          device bf16 [R_cap, H], rows in expert order: expert e
  *                   owns rows [expert_offsets[e], expert_offsets[e+1]), a
  *                   whole number of 128-row tiles (as ep_route_plan gives);
@@ -323,9 +324,10 @@ ep_status ep_nvfp4_colwise_rht_bf16(const void *x_bf16, int64_t R_cap,
 /*
  * ep_mxfp8_pack -- MXFP8 variant of the pack with the same routing gather.
  * TE PR #3270, description: bfloat16 tokens are quantised to MXFP8 and
- * dispatched; sequence diagram: "Quantize to E4M3 + E8M0 scales"; Changes:
- * "recv data and block scales share a single caller-supplied buffer, sliced
- * into data-then-scale regions".
+ * dispatched; sequence diagram: the quantisation step yields E4M3 data with
+ * E8M0 block scales; Changes: the received data and its block scales live in
+ * one buffer the caller provides, the data region first and the scales
+ * after it.
  *   buf             device u8: data [R_cap, H] then scales [R_cap, H/32].
  * Per 32-element block: e = smallest integer in [-127, 127] with
  * max|x| <= 448*2^e, scale byte e + 127, element E4M3_RNE(x / 2^e).

@@ -1,9 +1,10 @@
 // Columnwise RHT operand of a BF16 input with a supplied per-expert amax.
 //
 // TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the dGLU epilogue",
-// PR description: the rowwise amax is the exact amax of the dGLU epilogue
-// rounded to BF16, the post-RHT columnwise amax is bounded by 4x the rowwise
-// amax, and the separate grouped amax pass is skipped.  The input is the
+// PR description: the producer (the dGLU epilogue) already knows the exact
+// amax; its BF16 rounding is used as the rowwise amax, four times that bounds
+// every columnwise value after the RHT, and no separate amax pass over the
+// grouped tensor is made.  The input is the
 // expert-grouped BF16 gradient; the per-expert encode scale comes from the
 // supplied amax, so the data is read once.
 //

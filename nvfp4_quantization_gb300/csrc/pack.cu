@@ -1,9 +1,10 @@
 // Sender-side pack kernels with the routing gather fused in.
 //
 // NVFP4 (TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR
-// description: each token travels as one packed NVFP4 row of E2M1 codes, E4M3
-// block scales and a power-of-two FP32 token scale; the combine backward uses
-// stochastic rounding) and MXFP8 (TE PR #3270 "EP dispatch with unfused MXFP8
+// description: a token is quantised once and sent as a single row holding
+// E2M1 codes, an E4M3 scale for every 16 elements and an FP32 token scale that
+// is a power of two; in the combine backward the codes are stochastically
+// rounded) and MXFP8 (TE PR #3270 "EP dispatch with unfused MXFP8
 // quantization": E4M3 data with E8M0 scales per 32 elements, data and scales
 // in one buffer).
 //

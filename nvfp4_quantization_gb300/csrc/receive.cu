@@ -2,12 +2,13 @@
 // columnwise-RHT NVFP4 operands, in one pass over the rows' data.
 //
 // TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR description:
-// the receiver builds the NVFP4 GroupedTensor straight from the rows in one
-// pass; the rowwise operand reuses the sender's codes; the columnwise RHT
-// operand is quantised with a bound-derived per-expert scale (no BF16 round
-// trip, no amax pass over the data).  TE PR #3755 "Optionally derive FC1 dy
-// NVFP4 amaxes from the dGLU epilogue", PR description: the post-RHT
-// columnwise amax is bounded by 4x the rowwise amax.
+// the grouped NVFP4 operands are made directly from the received rows, reading
+// them once: rowwise, the codes the sender wrote are kept; columnwise, after
+// the RHT, values are requantised with a per-expert scale taken from a bound
+// rather than measured (nothing goes back through BF16).  TE PR #3755
+// "Optionally derive FC1 dy NVFP4 amaxes from the dGLU epilogue", PR
+// description: four times the rowwise amax bounds the columnwise amax after
+// the RHT.
 //
 // Work unit: a tile of 128 rows x 256 hidden columns (a tile never straddles
 // two experts: expert slots are multiples of 128 rows).  Persistent CTAs take

@@ -1,7 +1,7 @@
 // Decode packed NVFP4 rows to BF16: the path taken when direct receive is off
 // (TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR description:
-// "Otherwise the rows are decoded to BF16"; commit "grad direct-receive
-// opt-out": the opt-out returns the BF16 decode of the received rows).
+// without direct receive, the received rows go back to BF16; commit "grad
+// direct-receive opt-out": the opt-out hands back that BF16 decode).
 //
 // Unit of work: 8 consecutive elements of a row (4 code bytes, one E4M3
 // block scale, 16 bytes of BF16 out).  Consecutive threads take consecutive

@@ -131,8 +131,8 @@ uint16_t or_bf16_rne(double v)
 
 /* Token scale exponent (reading R3): the smallest integer k >= -126 with
  * amax <= 2688 * 2^k, where 2688 = 6 * 448 is the largest value a block can
- * hold (E2M1 max times E4M3 max).  TE PR #3753, PR description: "a
- * power-of-two FP32 token scale". */
+ * hold (E2M1 max times E4M3 max).  TE PR #3753, PR description: each token
+ * carries one FP32 scale, restricted to powers of two. */
 int or_token_scale_exp(double amax)
 {
     int k = -126;
@@ -143,7 +143,7 @@ int or_token_scale_exp(double amax)
 
 /* MXFP8 block exponent (reading R14): the smallest integer e in [-127, 127]
  * with bmax <= 448 * 2^e, so that no element saturates.  TE PR #3270, sequence
- * diagram: "Quantize to E4M3 + E8M0 scales". */
+ * diagram: the data is quantised to E4M3 with E8M0 block scales. */
 int or_mx_scale_exp(double bmax)
 {
     int e = -127;

@@ -3,9 +3,9 @@
  * oracle.h).
  *
  * TE PR #3270 "EP dispatch with unfused MXFP8 quantization": bfloat16 tokens
- * are quantised to MXFP8 ("E4M3 + E8M0 scales", sequence diagram; E4M3 only,
- * review thread) and "recv data and block scales share a single
- * caller-supplied buffer, sliced into data-then-scale regions" (Changes).
+ * are quantised to MXFP8 (E4M3 data with E8M0 block scales, sequence diagram;
+ * only E4M3, review thread), and the received data and its block scales sit
+ * in one buffer the caller provides, data first, scales after (Changes).
  *
  * Reading R14: 32-element blocks; the block exponent e is the smallest integer
  * in [-127, 127] with max|x| <= 448 * 2^e (no element saturates), stored as

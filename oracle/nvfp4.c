@@ -2,9 +2,10 @@
  * Oracle: NVFP4 row pack and unpack.  TEST INFRASTRUCTURE ONLY (see oracle.h).
  *
  * TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR description
- * and the review thread on the EP header comment: "the sender packs each token
- * into one NVFP4 row (E2M1 codes, E4M3 block scales and a power-of-two FP32
- * token scale)"; when direct receive is off "the rows are decoded to BF16".
+ * and the review thread on the EP header comment: a token is quantised once,
+ * on the sending side, into a single row of E2M1 codes with an E4M3 scale per
+ * 16 elements and an FP32 token scale that is a power of two; without direct
+ * receive the received rows are turned back into BF16.
  *
  * Row layout (reading R6), S = roundup16(9H/16 + 16) bytes:
  *   [0, H/2)        E2M1 codes, element 2i in the low nibble of byte i
@@ -30,8 +31,8 @@ static void put_u32(uint8_t *p, uint32_t v) { memcpy(p, &v, 4); }
 static float get_f32(const uint8_t *p) { float v; memcpy(&v, p, 4); return v; }
 
 /* Quantise one BF16 token into one packed row.
- *  A_t = max |x| (exact; TE PR #3755, test commit: the rowwise amaxes equal
- *        the amaxes of the BF16 input), S_t = 2^k_t (reading R3).
+ *  A_t = max |x| (exact; TE PR #3755, test commit: the test checks that each
+ *        rowwise amax is the BF16 input's own), S_t = 2^k_t (reading R3).
  *  s_b = E4M3_RNE_sat(B_b / (6 S_t)) with B_b the block's max |x| (R4).
  *  code = E2M1(x / (s_b S_t)), RNE or stochastic (R5, R13); s_b = 0 gives
  *        magnitude 0 with the sign kept (R2).

@@ -4,13 +4,13 @@
  * (see oracle.h).
  *
  * TE PR #3753 "Add NVFP4 EP dispatch and combine backward", PR description:
- * "the receiver builds the expert GEMM's NVFP4 GroupedTensor straight from the
- * rows in one pass: the rowwise operand reuses the sender's codes and the
- * columnwise RHT operand is quantized with a bound-derived per-expert scale,
- * so no BF16 round trip or amax pass is needed."
+ * the expert GEMM's grouped NVFP4 operands are made directly from the received
+ * rows, reading them once; the rowwise operand keeps the codes the sender
+ * wrote, and the RHT-transformed columnwise values are requantised with a
+ * per-expert scale that comes from a bound, so neither a BF16 round trip nor an amax pass is needed.
  * TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the dGLU
- * epilogue", PR description: "the post-RHT columnwise amax is bounded by 4x
- * the rowwise amax".
+ * epilogue", PR description: after the RHT no columnwise value exceeds four
+ * times the rowwise amax.
  * TE PR #3324 "Enable NVFP4 row-scaled (per-token) backward for
  * GroupedLinear", description: row-scaled (per-token) NVFP4 operands.
  */
@@ -175,9 +175,10 @@ void or_scale_swizzle(const uint8_t *lin, int64_t M, int64_t Kb, uint8_t *out)
 
 /* Columnwise RHT operand of a BF16 input with a supplied per-expert amax
  * (reading R24).  TE PR #3755 "Optionally derive FC1 dy NVFP4 amaxes from the
- * dGLU epilogue", PR description: the rowwise amax is the exact amax of the
- * dGLU epilogue rounded to BF16, the post-RHT columnwise amax is bounded by 4x
- * the rowwise amax, and the separate grouped amax pass is skipped.
+ * dGLU epilogue", PR description: the exact amax known to the dGLU epilogue,
+ * rounded to BF16, is the rowwise amax; four times it bounds the columnwise
+ * values after the RHT, so no separate amax pass over the grouped tensor is
+ * made.
  *   x        BF16 [R_cap][H], rows in expert order (expert e: rows
  *            [offsets[e], offsets[e+1]), a multiple of 16 rows)
  *   amax_in  [E] the supplied amax of each expert

@@ -1,6 +1,6 @@
 """Pins of the oracle's tiled scale-factor layout (reading R23: the layout of
-the "swizzled NVFP4 GroupedTensor" of TE PR #3753, commit "... under NVFP4
-autocast", taken as the 128-row x 4-column tiles that Blackwell block-scaled
+the grouped NVFP4 tensor with GEMM-swizzled scales of TE PR #3753, commit
+"... under NVFP4 autocast", taken as the 128-row x 4-column tiles that Blackwell block-scaled
 matrix multiplies read).
 
 The checks do not re-type the oracle's formula: positions worked out by hand
