@@ -165,6 +165,18 @@ ep_status ep_route_plan_noalloc(const int32_t *topk_idx, int64_t T, int k,
  *                   {f32 token scale S_t = 2^k, f32 token amax A_t,
  *                   u32 source token id, u32 0}.  A padding row is the packing
  *                   of an all-zero token with id 0xFFFFFFFF.
+ *   expert_amax     device f32 [E] or NULL.  When given, the token amax A_t of
+ *                   every row written is max-reduced into expert_amax[e] of
+ *                   the row's expert e (on the bit patterns: all values are
+ *                   >= 0), so that afterwards it holds the largest A_t over
+ *                   the rows of each expert (padding rows have A_t = 0): the
+ *                   per-expert amax ep_nvfp4_direct_receive can take instead
+ *                   of reducing the row trailers itself.  The caller fills it
+ *                   first (zeros, or the partial maxima of earlier packs into
+ *                   the same rows).  4-byte aligned.  With it, the next kernel
+ *                   on `stream` starts only after this call's kernel has
+ *                   finished (no early start under programmatic dependent
+ *                   launch).
  *   rounding        EP_ROUND_RNE or EP_ROUND_SR (element codes only; scales
  *                   are always round-to-nearest-even).  SR draws 8 bits per
  *                   element from Philox4x32-10 keyed by `seed`, counter
@@ -177,8 +189,8 @@ ep_status ep_nvfp4_pack(const void *tokens_bf16, int64_t T, int64_t H,
                         const int32_t *dest, int k,
                         const int32_t *expert_offsets,
                         const int32_t *expert_counts, int E, uint8_t *rows,
-                        int64_t R_cap, int rounding, uint64_t seed,
-                        uint32_t *dev_status, void *stream);
+                        int64_t R_cap, float *expert_amax, int rounding,
+                        uint64_t seed, uint32_t *dev_status, void *stream);
 
 /*
  * ep_nvfp4_dispatch -- ep_route_plan followed by ep_nvfp4_pack, in one call.
@@ -187,8 +199,10 @@ ep_status ep_nvfp4_pack(const void *tokens_bf16, int64_t T, int64_t H,
  * back on `stream`.
  *   Arguments: those of ep_route_plan (topk_idx, T, k, E, A, R_cap,
  *   expert_offsets, expert_counts, dest, workspace, ws_bytes) and of
- *   ep_nvfp4_pack (tokens_bf16, H, rows, rounding, seed); every check of both
- *   calls is made before anything is enqueued.  Outputs, device status and
+ *   ep_nvfp4_pack (tokens_bf16, H, rows, expert_amax, rounding, seed); every
+ *   check of both calls is made before anything is enqueued.  expert_amax
+ *   (f32 [E] or NULL) is set to zero by the routing kernel before the pack
+ *   max-reduces into it, so after the call it holds each expert's amax.  Outputs, device status and
  *   errors: exactly those of the two calls made in that order.
  *   Timing: the routing kernel starts only after all earlier work on `stream`
  *   has finished, so the pack kernel reads and encodes its first tokens while
@@ -200,8 +214,8 @@ ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16,
                             int64_t R_cap, int32_t *expert_offsets,
                             int32_t *expert_counts, int32_t *dest,
                             void *workspace, size_t ws_bytes, uint8_t *rows,
-                            int rounding, uint64_t seed, uint32_t *dev_status,
-                            void *stream);
+                            float *expert_amax, int rounding, uint64_t seed,
+                            uint32_t *dev_status, void *stream);
 
 /*
  * ep_nvfp4_unpack -- decode packed rows to BF16 (the path used when direct
@@ -242,6 +256,11 @@ typedef struct {
  * columnwise value exceeds four times the rowwise amax; TE PR #3324,
  * description: NVFP4 operands with one FP32 scale per row (per token).
  *   rows            device u8 [R_cap, S].
+ *   expert_amax     device f32 [E] or NULL: each expert's amax, the largest
+ *                   token amax A_t over its rows, already reduced (as
+ *                   ep_nvfp4_pack / ep_nvfp4_dispatch leave it); the outputs
+ *                   are then identical and no trailer pass is made.  NULL:
+ *                   the call reduces the trailers itself.  4-byte aligned.
  *   out             host pointer to the output descriptor.  The rowwise group
  *                   (rw_codes, rw_scales, rw_row_scale) may be all NULL to skip
  *                   it; everything else is required.
@@ -253,12 +272,14 @@ typedef struct {
  * and 16-row block: y = (1/4) H16 diag(sigma) d over the decoded values d;
  * s = E4M3_RNE_sat(max|y| * (S_enc/6)); code = E2M1(|y| * (S_enc/s)) with the
  * sign of y (FP32, single-rounded operations, in this order).
- * Two kernels on `stream`: the per-expert metadata from the row trailers (4
- * bytes per row), then the tile transform, which reads S_enc back.
+ * Kernels on `stream`: without expert_amax, the per-expert metadata from the
+ * row trailers (4 bytes per row), then the tile transform, which reads S_enc
+ * back; with it, the tile transform alone (it writes the metadata too).
  */
 ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
                                   int64_t H, const int32_t *expert_offsets,
-                                  int E, const ep_nvfp4_grouped *out,
+                                  int E, const float *expert_amax,
+                                  const ep_nvfp4_grouped *out,
                                   int rounding, uint64_t seed,
                                   uint16_t rht_sign_mask, uint32_t *dev_status,
                                   void *stream);
@@ -268,7 +289,8 @@ ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
  * tensors in the tiled layout that block-scaled GEMMs read.
  * TE PR #3753, commit "... under NVFP4 autocast": the combine backward hands
  * FC2's gradient over as a grouped NVFP4 tensor whose scales are already in
- * the GEMM's swizzled order and which carries GEMM operands only.  The pages do not spell the layout out; the one used is the
+ * the GEMM's swizzled order and which carries GEMM operands only.  The pages
+ * do not spell the layout out; the one used is the
  * Blackwell block-scaled operand layout: a scale matrix SF[M][Kb] is cut into
  * 512-byte tiles of 128 rows x 4 scale columns, tile (mt, kt) at byte
  * (mt*Kb/4 + kt)*512, and element (m, kb) of a tile at
@@ -283,7 +305,8 @@ ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap,
 ep_status ep_nvfp4_direct_receive_swizzled(const uint8_t *rows, int64_t R_cap,
                                            int64_t H,
                                            const int32_t *expert_offsets,
-                                           int E, const ep_nvfp4_grouped *out,
+                                           int E, const float *expert_amax,
+                                           const ep_nvfp4_grouped *out,
                                            int rounding, uint64_t seed,
                                            uint16_t rht_sign_mask,
                                            uint32_t *dev_status,

@@ -56,14 +56,14 @@ def _declare(L):
     L.ep_route_plan.restype = _I32
     L.ep_route_plan_noalloc.argtypes = [_P, _I64, _I32, _I32, _I32, _I64, _P, _P, _P, _P, _P]
     L.ep_route_plan_noalloc.restype = _I32
-    L.ep_nvfp4_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _I32, _U64, _P, _P]
+    L.ep_nvfp4_pack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _I32, _P, _I64, _P, _I32, _U64, _P, _P]
     L.ep_nvfp4_pack.restype = _I32
     L.ep_nvfp4_dispatch.argtypes = [_P, _P, _I64, _I64, _I32, _I32, _I32, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P,
-                                    _I32, _U64, _P, _P]
+                                    _P, _I32, _U64, _P, _P]
     L.ep_nvfp4_dispatch.restype = _I32
     L.ep_nvfp4_unpack.argtypes = [_P, _I64, _I64, _P, _I32, _P, _P, _P]
     L.ep_nvfp4_unpack.restype = _I32
-    L.ep_nvfp4_direct_receive.argtypes = [_P, _I64, _I64, _P, _I32, ctypes.POINTER(EpGrouped), _I32, _U64,
+    L.ep_nvfp4_direct_receive.argtypes = [_P, _I64, _I64, _P, _I32, _P, ctypes.POINTER(EpGrouped), _I32, _U64,
                                           ctypes.c_uint16, _P, _P]
     L.ep_nvfp4_direct_receive.restype = _I32
     L.ep_nvfp4_direct_receive_swizzled.argtypes = L.ep_nvfp4_direct_receive.argtypes

@@ -106,18 +106,29 @@ def ep_route_plan_noalloc(topk_idx: torch.Tensor, plan: RoutePlan, stream=None) 
     return plan
 
 
+def _need_amax(expert_amax, E: int):
+    if expert_amax is not None:
+        _need_cuda(expert_amax, "expert_amax", torch.float32)
+        if expert_amax.numel() < E:
+            raise ValueError("expert_amax needs E entries")
+
+
 def ep_nvfp4_pack(tokens: torch.Tensor, plan: RoutePlan, rows: torch.Tensor | None = None,
-                  rounding: int = EP_ROUND_RNE, seed: int = 0, stream=None) -> torch.Tensor:
-    """BF16 tokens [T, H] -> packed NVFP4 rows [R_cap, row_bytes(H)] (uint8)."""
+                  rounding: int = EP_ROUND_RNE, seed: int = 0, expert_amax: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """BF16 tokens [T, H] -> packed NVFP4 rows [R_cap, row_bytes(H)] (uint8).
+    ``expert_amax`` (f32 [E], filled by the caller, e.g. with zeros) receives
+    the max of the token amaxes of each expert's rows."""
     _need_cuda(tokens, "tokens", torch.bfloat16)
+    _need_amax(expert_amax, plan.E)
     T, H = tokens.shape
     S = row_bytes(H)
     if rows is None:
         rows = torch.empty((plan.R_cap, S), dtype=torch.uint8, device=tokens.device)
     _need_cuda(rows, "rows", torch.uint8)
     st = _lib.lib().ep_nvfp4_pack(_ptr(tokens), T, H, _ptr(plan.dest), plan.k, _ptr(plan.offsets),
-                                  _ptr(plan.counts), plan.E, _ptr(rows), rows.shape[0], int(rounding),
-                                  int(seed) & ((1 << 64) - 1), _ptr(plan.status), _stream(stream))
+                                  _ptr(plan.counts), plan.E, _ptr(rows), rows.shape[0], _ptr(expert_amax),
+                                  int(rounding), int(seed) & ((1 << 64) - 1), _ptr(plan.status), _stream(stream))
     check("ep_nvfp4_pack", st)
     return rows
 
@@ -126,10 +137,12 @@ def ep_nvfp4_dispatch(tokens: torch.Tensor, topk_idx: torch.Tensor, E: int, A: i
                       R_cap: int | None = None, plan: RoutePlan | None = None,
                       workspace: torch.Tensor | None = None, rows: torch.Tensor | None = None,
                       rounding: int = EP_ROUND_RNE, seed: int = 0, status: torch.Tensor | None = None,
-                      stream=None) -> tuple[RoutePlan, torch.Tensor]:
+                      expert_amax: torch.Tensor | None = None, stream=None) -> tuple[RoutePlan, torch.Tensor]:
     """ep_route_plan then ep_nvfp4_pack in one C call (the pack overlaps the
-    routing kernel); returns (plan, rows)."""
+    routing kernel); returns (plan, rows).  ``expert_amax`` (f32 [E]) is
+    zeroed and then receives each expert's amax, for ep_nvfp4_direct_receive."""
     _need_cuda(tokens, "tokens", torch.bfloat16)
+    _need_amax(expert_amax, E)
     _need_cuda(topk_idx, "topk_idx", torch.int32)
     T, k = topk_idx.shape
     if tokens.shape[0] != T:
@@ -152,8 +165,8 @@ def ep_nvfp4_dispatch(tokens: torch.Tensor, topk_idx: torch.Tensor, E: int, A: i
         raise ValueError("rows has fewer than R_cap rows")
     st = _lib.lib().ep_nvfp4_dispatch(_ptr(topk_idx), _ptr(tokens), T, H, k, E, A, R_cap, _ptr(plan.offsets),
                                       _ptr(plan.counts), _ptr(plan.dest), _ptr(workspace), workspace.numel() * 4,
-                                      _ptr(rows), int(rounding), int(seed) & ((1 << 64) - 1), _ptr(plan.status),
-                                      _stream(stream))
+                                      _ptr(rows), _ptr(expert_amax), int(rounding), int(seed) & ((1 << 64) - 1),
+                                      _ptr(plan.status), _stream(stream))
     check("ep_nvfp4_dispatch", st)
     return plan, rows
 
@@ -196,12 +209,16 @@ def grouped_struct(g: dict) -> EpGrouped:
 def ep_nvfp4_direct_receive(rows: torch.Tensor, H: int, offsets: torch.Tensor, E: int,
                             out: dict | None = None, rounding: int = EP_ROUND_RNE, seed: int = 0,
                             sign_mask: int = DEFAULT_SIGN_MASK, status: torch.Tensor | None = None,
-                            rowwise: bool = True, swizzled: bool = False, stream=None) -> dict:
+                            rowwise: bool = True, swizzled: bool = False, expert_amax: torch.Tensor | None = None,
+                            stream=None) -> dict:
     """Packed rows -> grouped rowwise + columnwise-RHT NVFP4 operands (dict of
     tensors, see ep_nvfp4_grouped in include/epq.h).  ``swizzled`` calls
     ep_nvfp4_direct_receive_swizzled: both scale tensors in the tiled layout
-    of block-scaled GEMM operands (H % 128 == 0)."""
+    of block-scaled GEMM operands (H % 128 == 0).  ``expert_amax`` (f32 [E]):
+    each expert's amax as the pack or dispatch reduced it; the call then
+    skips its own pass over the row trailers."""
     _need_cuda(rows, "rows", torch.uint8)
+    _need_amax(expert_amax, E)
     R_cap = rows.shape[0]
     if out is None:
         out = alloc_grouped(R_cap, H, E, rows.device, rowwise)
@@ -209,7 +226,8 @@ def ep_nvfp4_direct_receive(rows: torch.Tensor, H: int, offsets: torch.Tensor, E
         status = new_status(rows.device)
     desc = grouped_struct(out)
     name = "ep_nvfp4_direct_receive_swizzled" if swizzled else "ep_nvfp4_direct_receive"
-    st = getattr(_lib.lib(), name)(_ptr(rows), R_cap, H, _ptr(offsets), E, ctypes.byref(desc), int(rounding),
+    st = getattr(_lib.lib(), name)(_ptr(rows), R_cap, H, _ptr(offsets), E, _ptr(expert_amax), ctypes.byref(desc),
+                                   int(rounding),
                                    int(seed) & ((1 << 64) - 1), int(sign_mask) & 0xFFFF, _ptr(status),
                                    _stream(stream))
     check(name, st)

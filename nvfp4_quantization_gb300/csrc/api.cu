@@ -162,28 +162,35 @@ static ep_status pack_common_checks(const void *tokens, int64_t T, int64_t H, co
 
 ep_status ep_nvfp4_pack(const void *tokens_bf16, int64_t T, int64_t H, const int32_t *dest, int k,
                         const int32_t *expert_offsets, const int32_t *expert_counts, int E, uint8_t *rows,
-                        int64_t R_cap, int rounding, uint64_t seed, uint32_t *dev_status, void *stream)
+                        int64_t R_cap, float *expert_amax, int rounding, uint64_t seed, uint32_t *dev_status,
+                        void *stream)
 {
     int dev = -1;
     ep_status st = pack_common_checks(tokens_bf16, T, H, dest, k, expert_offsets, expert_counts, E, rows,
                                       R_cap, dev_status, &dev);
     if (st != EP_OK)
         return st;
+    if (!on_device(expert_amax, dev))
+        return EP_ERR_DEVICE;
+    if ((reinterpret_cast<uintptr_t>(expert_amax) & 3u) != 0)
+        return EP_ERR_ALIGN;
     if (rounding != EP_ROUND_RNE && rounding != EP_ROUND_SR)
         return EP_ERR_ARG;
     DeviceGuard g(dev);
     if (!g.ok)
         return EP_ERR_DEVICE;
     LaunchCtx c{(cudaStream_t)stream, dev, sm_count(dev)};
+    epq::PackAmax am;
+    am.amax = expert_amax;
     return cuda_status(epq::launch_nvfp4_pack(c, (const uint16_t *)tokens_bf16, (int)T, (int)H, dest, k,
                                               expert_offsets, expert_counts, E, rows, (int)R_cap, rounding,
-                                              seed, dev_status));
+                                              seed, dev_status, false, am));
 }
 
 ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16, int64_t T, int64_t H, int k, int E,
                             int A, int64_t R_cap, int32_t *expert_offsets, int32_t *expert_counts, int32_t *dest,
-                            void *workspace, size_t ws_bytes, uint8_t *rows, int rounding, uint64_t seed,
-                            uint32_t *dev_status, void *stream)
+                            void *workspace, size_t ws_bytes, uint8_t *rows, float *expert_amax, int rounding,
+                            uint64_t seed, uint32_t *dev_status, void *stream)
 {
     if (!expert_offsets || !expert_counts || !workspace || !dev_status || !rows ||
         (T > 0 && (!topk_idx || !dest || !tokens_bf16)))
@@ -191,7 +198,8 @@ ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16, in
     if (T < 0 || T * (int64_t)k > (int64_t)INT32_MAX || k < 1 || k > 32 || E < 1 || E > 1024 ||
         !shape_ok(T, H, k, E))
         return EP_ERR_SHAPE;
-    if (A <= 0 || A % 128 != 0 || !aligned16(tokens_bf16) || !aligned16(rows))
+    if (A <= 0 || A % 128 != 0 || !aligned16(tokens_bf16) || !aligned16(rows) ||
+        (reinterpret_cast<uintptr_t>(expert_amax) & 3u) != 0)
         return EP_ERR_ALIGN;
     if (R_cap < ep_rows_capacity(T, k, E, A) || R_cap > (int64_t)INT32_MAX)
         return EP_ERR_CAPACITY;
@@ -201,17 +209,23 @@ ep_status ep_nvfp4_dispatch(const int32_t *topk_idx, const void *tokens_bf16, in
         return EP_ERR_ARG;
     const int dev = device_of(expert_offsets);
     if (dev < 0 || !on_device(topk_idx, dev) || !on_device(tokens_bf16, dev) || !on_device(expert_counts, dev) ||
-        !on_device(dest, dev) || !on_device(workspace, dev) || !on_device(rows, dev) || !on_device(dev_status, dev))
+        !on_device(dest, dev) || !on_device(workspace, dev) || !on_device(rows, dev) || !on_device(dev_status, dev) ||
+        !on_device(expert_amax, dev))
         return EP_ERR_DEVICE;
     DeviceGuard g(dev);
     if (!g.ok)
         return EP_ERR_DEVICE;
     LaunchCtx c{(cudaStream_t)stream, dev, sm_count(dev)};
+    // the routing kernel zeroes expert_amax; the pack max-reduces into it,
+    // taking each slot's expert straight from topk_idx
     cudaError_t err = epq::launch_route_plan(c, topk_idx, (int)T, k, E, A, expert_offsets, expert_counts, dest,
-                                             (int32_t *)workspace, dev_status);
+                                             (int32_t *)workspace, dev_status, expert_amax);
+    epq::PackAmax am;
+    am.topk = topk_idx;
+    am.amax = expert_amax;
     if (err == cudaSuccess)
         err = epq::launch_nvfp4_pack(c, (const uint16_t *)tokens_bf16, (int)T, (int)H, dest, k, expert_offsets,
-                                     expert_counts, E, rows, (int)R_cap, rounding, seed, dev_status, true);
+                                     expert_counts, E, rows, (int)R_cap, rounding, seed, dev_status, true, am);
     return cuda_status(err);
 }
 
@@ -307,7 +321,8 @@ ep_status ep_nvfp4_unpack(const uint8_t *rows, int64_t R_cap, int64_t H, const i
 }
 
 static ep_status direct_receive_common(const uint8_t *rows, int64_t R_cap, int64_t H,
-                                       const int32_t *expert_offsets, int E, const ep_nvfp4_grouped *out,
+                                       const int32_t *expert_offsets, int E, const float *expert_amax,
+                                       const ep_nvfp4_grouped *out,
                                        int rounding, uint64_t seed, uint16_t rht_sign_mask, uint32_t *dev_status,
                                        void *stream, bool swz)
 {
@@ -326,13 +341,14 @@ static ep_status direct_receive_common(const uint8_t *rows, int64_t R_cap, int64
     if (rounding != EP_ROUND_RNE && rounding != EP_ROUND_SR)
         return EP_ERR_ARG;
     if (!aligned16(rows) || !aligned16(out->cw_codes) || !aligned16(out->cw_scales) ||
-        (rw_all && (!aligned16(out->rw_codes) || !aligned16(out->rw_scales))))
+        (rw_all && (!aligned16(out->rw_codes) || !aligned16(out->rw_scales))) ||
+        (reinterpret_cast<uintptr_t>(expert_amax) & 3u) != 0)
         return EP_ERR_ALIGN;
     const int dev = device_of(rows);
     if (dev < 0 || !on_device(expert_offsets, dev) || !on_device(dev_status, dev) ||
         !on_device(out->rw_codes, dev) || !on_device(out->rw_scales, dev) || !on_device(out->rw_row_scale, dev) ||
         !on_device(out->cw_codes, dev) || !on_device(out->cw_scales, dev) || !on_device(out->amax_row, dev) ||
-        !on_device(out->amax_col, dev) || !on_device(out->cw_scale_enc, dev))
+        !on_device(out->amax_col, dev) || !on_device(out->cw_scale_enc, dev) || !on_device(expert_amax, dev))
         return EP_ERR_DEVICE;
     DeviceGuard g(dev);
     if (!g.ok)
@@ -341,24 +357,24 @@ static ep_status direct_receive_common(const uint8_t *rows, int64_t R_cap, int64
     epq::GroupedOut o{out->rw_codes, out->rw_scales, out->rw_row_scale, out->cw_codes,
                       out->cw_scales, out->amax_row, out->amax_col, out->cw_scale_enc};
     return cuda_status(epq::launch_direct_receive(c, rows, (int)R_cap, (int)H, expert_offsets, E, o, rounding,
-                                                  seed, rht_sign_mask, dev_status, swz));
+                                                  seed, rht_sign_mask, dev_status, swz, expert_amax));
 }
 
 ep_status ep_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H, const int32_t *expert_offsets,
-                                  int E, const ep_nvfp4_grouped *out, int rounding, uint64_t seed,
-                                  uint16_t rht_sign_mask, uint32_t *dev_status, void *stream)
+                                  int E, const float *expert_amax, const ep_nvfp4_grouped *out, int rounding,
+                                  uint64_t seed, uint16_t rht_sign_mask, uint32_t *dev_status, void *stream)
 {
-    return direct_receive_common(rows, R_cap, H, expert_offsets, E, out, rounding, seed, rht_sign_mask, dev_status,
-                                 stream, false);
+    return direct_receive_common(rows, R_cap, H, expert_offsets, E, expert_amax, out, rounding, seed, rht_sign_mask,
+                                 dev_status, stream, false);
 }
 
 ep_status ep_nvfp4_direct_receive_swizzled(const uint8_t *rows, int64_t R_cap, int64_t H,
-                                           const int32_t *expert_offsets, int E, const ep_nvfp4_grouped *out,
-                                           int rounding, uint64_t seed, uint16_t rht_sign_mask,
-                                           uint32_t *dev_status, void *stream)
+                                           const int32_t *expert_offsets, int E, const float *expert_amax,
+                                           const ep_nvfp4_grouped *out, int rounding, uint64_t seed,
+                                           uint16_t rht_sign_mask, uint32_t *dev_status, void *stream)
 {
-    return direct_receive_common(rows, R_cap, H, expert_offsets, E, out, rounding, seed, rht_sign_mask, dev_status,
-                                 stream, true);
+    return direct_receive_common(rows, R_cap, H, expert_offsets, E, expert_amax, out, rounding, seed, rht_sign_mask,
+                                 dev_status, stream, true);
 }
 
 } // extern "C"

@@ -78,8 +78,8 @@ colwise_rht_bf16_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const 
     // S_enc = min(2688 / amax_col, FLT_MAX) (1 when amax_col = 0)
     for (int e = tid; e < E; e += kCbThreads) {
         const float a = round_bf16(__ldg(amax_in + e));
-        const float ac = 4.0f * a;
-        const float se = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
+        float ac;
+        const float se = colwise_encode_scale(a, ac);
         se_s[e] = se;
         if (blockIdx.x == 0) {
             amax_row[e] = a;

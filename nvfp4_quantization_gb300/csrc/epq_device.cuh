@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <float.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -150,6 +151,39 @@ __device__ __forceinline__ void raise_status(uint32_t *st, uint32_t bits)
 {
     if (st)
         atomicOr(st, bits);
+}
+
+// ---------------------------------------------------------------- per-expert amax
+// Max-reduction of a non-negative FP32 value into *p, done on the bit
+// patterns: for non-negative floats the unsigned order of the bits is the
+// numeric order.  Fire-and-forget (no value comes back).
+__device__ __forceinline__ void red_max_nonneg(float *p, float v)
+{
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(__float_as_uint(v)) : "memory");
+}
+
+// The expert whose slot holds row d: the last e with offsets[e] <= d (empty
+// slots before it share its offset and are skipped by taking the last).
+__device__ __forceinline__ int expert_of_dest(const int32_t *__restrict__ offsets, int E, int d)
+{
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(offsets + mid) <= d)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Columnwise metadata of an expert from its rowwise amax A_e (reading R11):
+// amax_col = fl32(4 A_e), S_enc = min(fl32(2688 / amax_col), FLT_MAX), and
+// S_enc = 1 for an expert whose amax is 0 (no rows, or all-zero rows).
+__device__ __forceinline__ float colwise_encode_scale(float amax_row, float &amax_col)
+{
+    amax_col = 4.0f * amax_row;
+    return amax_col > 0.0f ? fminf(__fdiv_rn(2688.0f, amax_col), FLT_MAX) : 1.0f;
 }
 
 // ---------------------------------------------------------------- mbarrier

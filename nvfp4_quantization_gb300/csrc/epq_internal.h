@@ -58,16 +58,29 @@ cudaError_t ensure_smem_limit(K kernel, int device, int bytes, std::atomic<uint3
 size_t route_workspace_bytes(int64_t T, int E);
 // Launched without programmatic dependency: it starts only once every earlier
 // kernel on the stream has finished (launch_nvfp4_pack's `early` relies on it).
+// amax_zero (optional, f32 [E]): set to 0 by the kernel, for a pack that
+// max-reduces the per-expert amax into it.
 cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, int k, int E, int A,
                               int32_t *offsets, int32_t *counts, int32_t *dest, int32_t *hist,
-                              uint32_t *status);
+                              uint32_t *status, float *amax_zero = nullptr);
+
+// The pack's optional per-expert amax: every written row's token amax A_t is
+// max-reduced into amax[e] of its expert e (the array holds zeros, or an
+// earlier partial max, when the pack starts).  topk, when given, names the
+// expert of each (token, slot) directly; otherwise it is found from the row
+// index and the expert offsets.
+struct PackAmax {
+    const int32_t *topk = nullptr;
+    float *amax = nullptr;
+};
 
 // early: the launch directly follows launch_route_plan on the same stream,
 // so the tokens may be read before the wait for the routing kernel.
 cudaError_t launch_nvfp4_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                               const int32_t *dest, int k, const int32_t *offsets,
                               const int32_t *counts, int E, uint8_t *rows, int R_cap,
-                              int rounding, uint64_t seed, uint32_t *status, bool early = false);
+                              int rounding, uint64_t seed, uint32_t *status, bool early = false,
+                              PackAmax am = PackAmax());
 
 cudaError_t launch_mxfp8_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                               const int32_t *dest, int k, const int32_t *offsets,
@@ -101,7 +114,7 @@ cudaError_t launch_mxfp8_colwise(const LaunchCtx &c, const uint16_t *x, int R_ca
 cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
                                   const int32_t *offsets, int E, const GroupedOut &out,
                                   int rounding, uint64_t seed, uint32_t sign_mask,
-                                  uint32_t *status, bool swz = false);
+                                  uint32_t *status, bool swz = false, const float *amax_in = nullptr);
 
 // Bytes of a packed NVFP4 row: roundup16(9H/16 + 16).
 inline int64_t row_bytes(int64_t H) { return (9 * H / 16 + 16 + 15) / 16 * 16; }

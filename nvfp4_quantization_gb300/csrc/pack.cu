@@ -249,11 +249,13 @@ nvfp4_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
                   int k, const int32_t *__restrict__ offsets, const int32_t *__restrict__ counts, int E,
                   uint8_t *__restrict__ rows, int64_t S, int R_cap, const __grid_constant__ PhiloxKey key,
                   uint32_t *__restrict__ status, int n_tok_ctas, int pad_ctas,
-                  const __grid_constant__ RcpTable rcp)
+                  const __grid_constant__ RcpTable rcp, const int32_t *__restrict__ topk,
+                  float *__restrict__ expert_amax)
 {
     __shared__ uint32_t wmax[2][kMaxThreads / 32];
     __shared__ float srcp[128];
-    pdl_launch_dependents();
+    if (!expert_amax)   // as in the warp kernel: a reader of the amax starts after this grid
+        pdl_launch_dependents();
     pdl_wait();
     if ((int)blockIdx.x >= n_tok_ctas) {
         fill_padding(0, blockIdx.x - n_tok_ctas, pad_ctas, offsets, counts, E, R_cap, rows, S, H, status);
@@ -350,6 +352,15 @@ nvfp4_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
                     *reinterpret_cast<uint16_t *>(row + o) = 0;
             }
         }
+        // thread j: slot j's expert takes A_t into its max
+        if (expert_amax && (int)threadIdx.x < k) {
+            const int d = __ldg(dest + (int64_t)t * k + threadIdx.x);
+            if (d >= 0 && d < R_cap) {
+                const int e = topk ? __ldg(topk + (int64_t)t * k + threadIdx.x) : expert_of_dest(offsets, E, d);
+                if (e >= 0 && e < E)
+                    red_max_nonneg(expert_amax + e, u2f(a_bits << 16));
+            }
+        }
         if (tn < T) {
 #pragma unroll
             for (int c = 0; c < CPT; ++c)
@@ -428,12 +439,17 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
                        int k, const int32_t *__restrict__ offsets, const int32_t *__restrict__ counts, int E,
                        uint8_t *__restrict__ rows, int64_t S, int R_cap, const __grid_constant__ PhiloxKey key,
                        uint32_t *__restrict__ status, int n_tok_ctas, int pad_ctas,
-                       const __grid_constant__ RcpTable rcp, int early)
+                       const __grid_constant__ RcpTable rcp, int early, const int32_t *__restrict__ topk,
+                       float *__restrict__ expert_amax)
 {
     extern __shared__ __align__(128) uint8_t pbuf[];   // [kPackWarps][kBuf][2H]
     __shared__ float srcp[128];
     __shared__ uint64_t bar[kPackWarps][kBuf];
-    pdl_launch_dependents();
+    // With the per-expert amax reduced here, the next kernel (a direct receive
+    // that reads it) is let in only when this grid is done: started earlier,
+    // its CTAs would sit on the SMs this grid's last CTAs still need.
+    if (!expert_amax)
+        pdl_launch_dependents();
     if ((int)blockIdx.x >= n_tok_ctas) {
         pdl_wait();
         fill_padding(0, blockIdx.x - n_tok_ctas, pad_ctas, offsets, counts, E, R_cap, rows, S, H, status);
@@ -556,6 +572,13 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
                 for (int64_t o = 9 * (int64_t)H / 16; o < S - 16; o += 2)
                     *reinterpret_cast<uint16_t *>(row + o) = 0;
         }
+        // the expert of each written row takes the token amax A_t into its max
+        // (lane j: slot j; the routing plan zeroed the array, or the caller did)
+        if (expert_amax && lane < k && dl >= 0 && dl < R_cap) {
+            const int e = topk ? __ldg(topk + (int64_t)t * k + lane) : expert_of_dest(offsets, E, dl);
+            if (e >= 0 && e < E)
+                red_max_nonneg(expert_amax + e, u2f(a_bits << 16));
+        }
     }
 }
 
@@ -651,7 +674,7 @@ template <int CPT>
 static cudaError_t launch_nvfp4_cpt(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                                     const int32_t *dest, int k, const int32_t *offsets,
                                     const int32_t *counts, int E, uint8_t *rows, int R_cap,
-                                    int rounding, uint64_t seed, uint32_t *status)
+                                    int rounding, uint64_t seed, uint32_t *status, PackAmax am)
 {
     static const RcpTable rcp = make_rcp_table();
     const int th = pack_threads(H, CPT);
@@ -666,16 +689,17 @@ static cudaError_t launch_nvfp4_cpt(const LaunchCtx &c, const uint16_t *tokens, 
         tc = 1;
     if (rounding == 1)
         return launch_pdl(nvfp4_pack_kernel<CPT, true>, dim3(tc + pc), dim3(th), 0, c.stream, tokens, T, H, dest,
-                          k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
+                          k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, am.topk,
+                          am.amax);
     return launch_pdl(nvfp4_pack_kernel<CPT, false>, dim3(tc + pc), dim3(th), 0, c.stream, tokens, T, H, dest, k,
-                      offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp);
+                      offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, am.topk, am.amax);
 }
 
 template <int NB>
 static cudaError_t launch_nvfp4_warp(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                                      const int32_t *dest, int k, const int32_t *offsets,
                                      const int32_t *counts, int E, uint8_t *rows, int R_cap,
-                                     int rounding, uint64_t seed, uint32_t *status, int early)
+                                     int rounding, uint64_t seed, uint32_t *status, int early, PackAmax am)
 {
     static const RcpTable rcp = make_rcp_table();
     const int pc = padding_ctas(c, E);
@@ -703,19 +727,21 @@ static cudaError_t launch_nvfp4_warp(const LaunchCtx &c, const uint16_t *tokens,
         tc = 1;
     if (rounding == 1)
         return launch_pdl(nvfp4_pack_warp_kernel<NB, true>, dim3(tc + pc), dim3(th), smem, c.stream, tokens, T, H,
-                          dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, early);
+                          dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, early,
+                          am.topk, am.amax);
     return launch_pdl(nvfp4_pack_warp_kernel<NB, false>, dim3(tc + pc), dim3(th), smem, c.stream, tokens, T, H,
-                      dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, early);
+                      dest, k, offsets, counts, E, rows, S, R_cap, philox_key(seed), status, tc, pc, rcp, early,
+                      am.topk, am.amax);
 }
 
 cudaError_t launch_nvfp4_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,
                               const int32_t *dest, int k, const int32_t *offsets,
                               const int32_t *counts, int E, uint8_t *rows, int R_cap,
-                              int rounding, uint64_t seed, uint32_t *status, bool early)
+                              int rounding, uint64_t seed, uint32_t *status, bool early, PackAmax am)
 {
     if (H % 512 == 0 && H <= 8192) {
         switch (H / 512) {
-#define EPQ_NB(n) case n: return launch_nvfp4_warp<n>(c, tokens, T, H, dest, k, offsets, counts, E, rows, R_cap, rounding, seed, status, early ? 1 : 0);
+#define EPQ_NB(n) case n: return launch_nvfp4_warp<n>(c, tokens, T, H, dest, k, offsets, counts, E, rows, R_cap, rounding, seed, status, early ? 1 : 0, am);
             EPQ_NB(1) EPQ_NB(2) EPQ_NB(3) EPQ_NB(4) EPQ_NB(5) EPQ_NB(6) EPQ_NB(7) EPQ_NB(8)
             EPQ_NB(9) EPQ_NB(10) EPQ_NB(11) EPQ_NB(12) EPQ_NB(13) EPQ_NB(14) EPQ_NB(15) EPQ_NB(16)
 #undef EPQ_NB
@@ -725,12 +751,12 @@ cudaError_t launch_nvfp4_pack(const LaunchCtx &c, const uint16_t *tokens, int T,
     const int nq = H / 32;
     if (nq <= kMaxThreads)
         return launch_nvfp4_cpt<1>(c, tokens, T, H, dest, k, offsets, counts, E, rows, R_cap,
-                                   rounding, seed, status);
+                                   rounding, seed, status, am);
     if (nq <= 2 * kMaxThreads)
         return launch_nvfp4_cpt<2>(c, tokens, T, H, dest, k, offsets, counts, E, rows, R_cap,
-                                   rounding, seed, status);
+                                   rounding, seed, status, am);
     return launch_nvfp4_cpt<4>(c, tokens, T, H, dest, k, offsets, counts, E, rows, R_cap, rounding,
-                               seed, status);
+                               seed, status, am);
 }
 
 cudaError_t launch_mxfp8_pack(const LaunchCtx &c, const uint16_t *tokens, int T, int H,

@@ -113,7 +113,7 @@ struct DrArgs {
     float *rw_row_scale;
     uint8_t *cw_codes;
     uint8_t *cw_scales;
-    const float *scale_enc;
+    float *scale_enc;
     PhiloxKey key;     // round keys of the SR seed
     uint32_t sign_mask;
     uint32_t *status;
@@ -121,6 +121,11 @@ struct DrArgs {
     int cw_v8;         // cw_codes is 32-byte aligned: 32-byte stores
     float rcp[128];    // RN(1 / s) for every E4M3 code s (0 for s = 0), computed on the host
     int rws_tma;       // rowwise scales leave by TMA store (H % 256 == 0)
+    // per-expert amax reduced by the pack (else S_enc comes from the amax
+    // kernel through scale_enc); last, so the fields above keep their offsets
+    // (moving them made the SR kernel spill)
+    const float *amax_in;
+    float *amax_row, *amax_col;
 };
 
 // Tiles of a CTA: u = blockIdx.x + k * gridDim.x, k = 0, 1, ... over the tiles
@@ -218,10 +223,12 @@ expert_amax_kernel(const uint8_t *__restrict__ rows, int64_t S, const int32_t *_
             uint32_t x = 0u;
             for (int w = 0; w < kAmaxThreads / 32; ++w)
                 x = max(x, red[w]);
-            const float a = u2f(x), ac = 4.0f * a;
+            const float a = u2f(x);
+            float ac;
+            const float se = colwise_encode_scale(a, ac);
             amax_row[e] = a;
             amax_col[e] = ac;
-            scale_enc[e] = ac > 0.0f ? fminf(__fdiv_rn(2688.0f, ac), FLT_MAX) : 1.0f;
+            scale_enc[e] = se;
         }
         __syncthreads();
     }
@@ -633,9 +640,11 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     // The other stages are loaded once it has arrived, so that at start-up,
     // when every CTA asks at once, first tiles are not queued behind second
     // ones.
+    // With the amax supplied (p.amax_in) the grid before this one is the pack
+    // itself, and no row may be read before the wait on it.
     const int rt0 = (int)blockIdx.x / p.n_strips, st0 = (int)blockIdx.x % p.n_strips;
     const int pre = rt0 < p.R_cap / kTileRows ? 1 : 0;
-    if (threadIdx.x == 0 && pre)
+    if (threadIdx.x == 0 && pre && !p.amax_in)
         issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, 0, rt0, st0);
     __syncthreads();
     pdl_launch_dependents();
@@ -655,9 +664,24 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const bool use0 = (int)blockIdx.x < n_units;   // tile 0 holds rows in use
 
     pdl_wait();
-    for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
-        const float se = p.scale_enc[i];
-        sm.se_cache[i] = se;
+    if (threadIdx.x == 0 && pre && p.amax_in)
+        issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, 0, rt0, st0);
+    if (p.amax_in) {
+        // S_enc of every expert from the supplied amax; CTA 0 writes the metadata
+        for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
+            const float a = p.amax_in[i];
+            float ac;
+            const float se = colwise_encode_scale(a, ac);
+            sm.se_cache[i] = se;
+            if (blockIdx.x == 0) {
+                p.amax_row[i] = a;
+                p.amax_col[i] = ac;
+                p.scale_enc[i] = se;
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < p.E; i += blockDim.x)
+            sm.se_cache[i] = p.scale_enc[i];
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -731,12 +755,18 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
 cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R_cap, int H,
                                   const int32_t *offsets, int E, const GroupedOut &out,
                                   int rounding, uint64_t seed, uint32_t sign_mask,
-                                  uint32_t *status, bool swz)
+                                  uint32_t *status, bool swz, const float *amax_in)
 {
     const int64_t S = row_bytes(H);
-    cudaError_t err = launch_pdl(expert_amax_kernel, dim3((unsigned)E), dim3(kAmaxThreads), 0, c.stream, rows, S,
-                                 offsets, E, R_cap, out.amax_row, out.amax_col, out.scale_enc);
-    if (err != cudaSuccess || R_cap < kTileRows)   // fewer than 128 rows of capacity: no tile can exist
+    // fewer than 128 rows of capacity: no tile can exist, and the amax kernel
+    // alone writes the metadata (from the trailers: the same values)
+    if (R_cap < kTileRows)
+        amax_in = nullptr;
+    cudaError_t err = cudaSuccess;
+    if (!amax_in)
+        err = launch_pdl(expert_amax_kernel, dim3((unsigned)E), dim3(kAmaxThreads), 0, c.stream, rows, S, offsets, E,
+                         R_cap, out.amax_row, out.amax_col, out.scale_enc);
+    if (err != cudaSuccess || R_cap < kTileRows)
         return err;
 
     CUtensorMap tm_codes, tm_scales, tm_trailer, tm_rw, tm_rws;
@@ -768,6 +798,9 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     a.cw_codes = out.cw_codes;
     a.cw_scales = out.cw_scales;
     a.scale_enc = out.scale_enc;
+    a.amax_in = amax_in;
+    a.amax_row = out.amax_row;
+    a.amax_col = out.amax_col;
     a.key = philox_key(seed);
     a.sign_mask = sign_mask;
     a.status = status;

@@ -135,9 +135,13 @@ template <bool kCluster>
 __global__ void __launch_bounds__(kChunk)
 route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A,
                       int32_t *__restrict__ offsets, int32_t *__restrict__ counts, int32_t *__restrict__ dest,
-                      uint32_t *__restrict__ ws, uint32_t *__restrict__ status)
+                      uint32_t *__restrict__ ws, uint32_t *__restrict__ status, float *__restrict__ amax_zero)
 {
     extern __shared__ uint32_t sm[];
+    // the per-expert amax the pack that follows max-reduces into starts at 0
+    if (amax_zero && blockIdx.x == 0)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            amax_zero[e] = 0.0f;
     uint32_t *mask = sm;                         // [E][kWords]
     uint32_t *pre = mask + (size_t)E * kWords;   // [E][kWords]
     int *tot = reinterpret_cast<int *>(pre + (size_t)E * kWords);  // [E]
@@ -274,9 +278,12 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
 __global__ void __launch_bounds__(kChunk)
 route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, int chunks_per_cta,
                   int32_t *__restrict__ offsets, int32_t *__restrict__ counts, int32_t *__restrict__ dest,
-                  uint32_t *__restrict__ ws, uint32_t *__restrict__ status)
+                  uint32_t *__restrict__ ws, uint32_t *__restrict__ status, float *__restrict__ amax_zero)
 {
     extern __shared__ uint32_t sm[];
+    if (amax_zero && blockIdx.x == 0)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            amax_zero[e] = 0.0f;
     uint32_t *mask = sm;                         // [E][kWords]
     uint32_t *pre = mask + (size_t)E * kWords;   // [E][kWords]
     int *run = reinterpret_cast<int *>(pre + (size_t)E * kWords);  // [E]
@@ -414,7 +421,7 @@ size_t route_workspace_bytes(int64_t T, int E)
 
 cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, int k, int E, int A,
                               int32_t *offsets, int32_t *counts, int32_t *dest, int32_t *hist,
-                              uint32_t *status)
+                              uint32_t *status, float *amax_zero)
 {
     const size_t smem = (size_t)E * kWords * 4u * 2u + (size_t)E * 4u * 4u;
     static std::atomic<uint32_t> done[2] = {}, done_reg[2] = {}, done_cl[2] = {};
@@ -484,13 +491,13 @@ cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, in
         }
         if (ok)
             return cudaLaunchKernelEx(&ccfg, route_plan_reg_kernel<true>, topk, T, k, E, A, offsets, counts, dest,
-                                      reinterpret_cast<uint32_t *>(hist), status);
+                                      reinterpret_cast<uint32_t *>(hist), status, amax_zero);
     }
     if (cpc == 1 && k <= kRegSlots)
         return cudaLaunchKernelEx(&cfg, route_plan_reg_kernel<false>, topk, T, k, E, A, offsets, counts, dest,
-                                  reinterpret_cast<uint32_t *>(hist), status);
+                                  reinterpret_cast<uint32_t *>(hist), status, amax_zero);
     return cudaLaunchKernelEx(&cfg, route_plan_kernel, topk, T, k, E, A, cpc, offsets, counts, dest,
-                              reinterpret_cast<uint32_t *>(hist), status);
+                              reinterpret_cast<uint32_t *>(hist), status, amax_zero);
 }
 
 } // namespace epq

@@ -30,9 +30,19 @@ def assert_bytes_equal(got: np.ndarray, want: np.ndarray, what: str):
 class GpuRun:
     """The hot path on the GPU for one workload, with canary-filled outputs."""
 
-    def __init__(self, w, rowwise=True, mxfp8=False, unpack=False, R_cap=None, dispatch=False, swizzled=False):
+    def __init__(self, w, rowwise=True, mxfp8=False, unpack=False, R_cap=None, dispatch=False, swizzled=False,
+                 amax=False):
+        """amax: the pack (or dispatch) reduces the per-expert amax, and the
+        direct receive takes it instead of reducing the row trailers."""
         self.w = w
         self.swizzled = swizzled
+        self.expert_amax = None
+        if amax:
+            # canary bits where the dispatch's routing kernel must write zeros;
+            # the separate pack accumulates into what the caller put there
+            self.expert_amax = torch.full((w.E,), 0.0, dtype=torch.float32, device="cuda")
+            if dispatch:
+                self.expert_amax.view(torch.int32).fill_(0x7F7F7F7F)
         self.tok = to_dev_bf16(w.tokens)
         self.topk = torch.from_numpy(np.ascontiguousarray(w.topk)).cuda()
         self.R_cap = R_cap or nq.rows_capacity(w.T, w.k, w.E, w.A)
@@ -40,16 +50,18 @@ class GpuRun:
         self.rows = torch.full((self.R_cap, S), CANARY, dtype=torch.uint8, device="cuda")
         if dispatch:   # route plan + pack in one call
             self.plan, _ = nq.ep_nvfp4_dispatch(self.tok, self.topk, w.E, w.A, R_cap=self.R_cap, rows=self.rows,
-                                                rounding=w.rounding, seed=w.seed)
+                                                rounding=w.rounding, seed=w.seed, expert_amax=self.expert_amax)
         else:
             self.plan = nq.ep_route_plan(self.topk, w.E, w.A, R_cap=self.R_cap)
-            nq.ep_nvfp4_pack(self.tok, self.plan, rows=self.rows, rounding=w.rounding, seed=w.seed)
+            nq.ep_nvfp4_pack(self.tok, self.plan, rows=self.rows, rounding=w.rounding, seed=w.seed,
+                             expert_amax=self.expert_amax)
         g = nq.alloc_grouped(self.R_cap, w.H, w.E, "cuda", rowwise=rowwise)
         for t in g.values():
             t.view(torch.uint8).fill_(CANARY)
         self.grouped = nq.ep_nvfp4_direct_receive(self.rows, w.H, self.plan.offsets, w.E, out=g,
                                                   rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask,
-                                                  status=self.plan.status, swizzled=swizzled)
+                                                  status=self.plan.status, swizzled=swizzled,
+                                                  expert_amax=self.expert_amax)
         self.unpacked = None
         if unpack:
             self.unpacked = torch.full((self.R_cap, w.H), 0, dtype=torch.bfloat16, device="cuda")
@@ -98,6 +110,9 @@ def compare_runs(g: GpuRun, o: OracleRun, check_rowwise=True):
     for name in ("amax_row", "amax_col", "cw_scale_enc"):
         oname = "scale_enc" if name == "cw_scale_enc" else name
         assert_bytes_equal(gr[name].view(np.uint32), o.dr[oname].view(np.uint32), name)
+    if g.expert_amax is not None:   # the pack's reduction is the receive's rowwise amax
+        assert_bytes_equal(g.host(g.expert_amax).view(np.uint32), o.dr["amax_row"].view(np.uint32),
+                           "expert_amax from the pack")
     assert_bytes_equal(gr["cw_codes"][: R * H // 2], o.dr["cw_codes"][: R * H // 2], "columnwise codes")
     assert_bytes_equal(gr["cw_scales"][: R * H // 16], odr["cw_scales"][: R * H // 16], "columnwise scales")
     assert (gr["cw_codes"][R * H // 2:] == CANARY).all()

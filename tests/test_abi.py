@@ -73,10 +73,10 @@ def test_pack_validation():
 
     def call(**kw):
         a = dict(tok=FAKE, T=4, H=1024, dest=FAKE, k=2, off=FAKE, cnt=FAKE, E=4, rows=FAKE, R_cap=600,
-                 rnd=0, seed=0, st=FAKE)
+                 amax=None, rnd=0, seed=0, st=FAKE)
         a.update(kw)
         return L.ep_nvfp4_pack(a["tok"], a["T"], a["H"], a["dest"], a["k"], a["off"], a["cnt"], a["E"], a["rows"],
-                               a["R_cap"], a["rnd"], a["seed"], a["st"], None)
+                               a["R_cap"], a["amax"], a["rnd"], a["seed"], a["st"], None)
     assert call(rows=None) == -1
     assert call(H=1000) == -2 and call(H=0) == -2 and call(k=40) == -2
     assert call(R_cap=-1) == -4
@@ -85,17 +85,32 @@ def test_pack_validation():
     assert L.ep_mxfp8_pack(FAKE, 4, 48, FAKE, 2, FAKE, FAKE, 4, FAKE, 600, FAKE, None) == -2
 
 
+def test_dispatch_validation():
+    L = nq.lib()
+    bad = ctypes.c_void_p(0x10002)
+    args = [FAKE, FAKE, 4, 1024, 2, 4, 128, 600, FAKE, FAKE, FAKE, FAKE, 1 << 20, FAKE]
+    assert L.ep_nvfp4_dispatch(*args, bad, 0, 0, FAKE, None) == -3        # misaligned expert_amax
+    assert L.ep_nvfp4_dispatch(*args, None, 7, 0, FAKE, None) == -5       # unknown rounding
+    args[6] = 64
+    assert L.ep_nvfp4_dispatch(*args, None, 0, 0, FAKE, None) == -3       # alignment A not a multiple of 128
+
+
 def test_receive_and_unpack_validation():
     L = nq.lib()
     g = _lib.EpGrouped()
-    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, ctypes.byref(g), 0, 0, 0, FAKE, None) == -1
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, None, ctypes.byref(g), 0, 0, 0, FAKE, None) == -1
     g = _lib.EpGrouped(rw_codes=FAKE.value, cw_codes=FAKE.value, cw_scales=FAKE.value, amax_row=FAKE.value,
                        amax_col=FAKE.value, cw_scale_enc=FAKE.value)
     # a partial rowwise group is rejected
-    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, ctypes.byref(g), 0, 0, 0, FAKE, None) == -1
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, None, ctypes.byref(g), 0, 0, 0, FAKE, None) == -1
     g.rw_codes = None
-    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1000, FAKE, 4, ctypes.byref(g), 0, 0, 0, FAKE, None) == -2
-    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, ctypes.byref(g), 7, 0, 0, FAKE, None) == -5
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1000, FAKE, 4, None, ctypes.byref(g), 0, 0, 0, FAKE, None) == -2
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, None, ctypes.byref(g), 7, 0, 0, FAKE, None) == -5
+    # a supplied per-expert amax must be 4-byte aligned
+    bad = ctypes.c_void_p(0x10002)
+    assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, bad, ctypes.byref(g), 0, 0, 0, FAKE, None) == -3
+    assert L.ep_nvfp4_direct_receive_swizzled(FAKE, 128, 1024, FAKE, 4, bad, ctypes.byref(g), 0, 0, 0, FAKE,
+                                              None) == -3
     assert L.ep_nvfp4_unpack(FAKE, 128, 1000, FAKE, 4, FAKE, FAKE, None) == -2
     assert L.ep_nvfp4_unpack(None, 128, 1024, FAKE, 4, FAKE, FAKE, None) == -1
 

@@ -439,3 +439,76 @@ def test_parity_wide_hidden():
     g = GpuRun(w, unpack=True, mxfp8=True)
     o = OracleRun(w, g.R_cap, unpack=True, mxfp8=True)
     compare_runs(g, o)
+
+
+@pytest.mark.parametrize("name,dispatch", [("cfg1", True), ("cfg2", True), ("cfg4", True), ("cfg5", False),
+                                           ("cfg1_ragged_H", True), ("cfg4_ragged_H", False), ("cfg4", False)])
+def test_parity_pack_reduced_amax(name, dispatch):
+    """The per-expert amax max-reduced by the pack as it writes the rows
+    (through ep_nvfp4_dispatch, which zeroes it in the routing kernel and
+    names each slot's expert from topk_idx; or through ep_nvfp4_pack, which
+    finds the expert from the row index) equals the oracle's rowwise amax bit
+    for bit, and the direct receive given it (no trailer pass, the tile
+    kernel writes the metadata) produces the same operands.  The ragged-H
+    cases take the general pack kernel."""
+    c = CASES[name]
+    w = workloads.make(c["cfg"], **c["kw"])
+    g = GpuRun(w, unpack=c.get("unpack", False), dispatch=dispatch, amax=True)
+    o = OracleRun(w, g.R_cap, unpack=c.get("unpack", False))
+    compare_runs(g, o)
+
+
+def test_parity_pack_reduced_amax_swizzled_and_edges():
+    # the tiled-scale receive with the supplied amax
+    w = workloads.make(2, T=600, H=1024)
+    compare_runs(GpuRun(w, swizzled=True, dispatch=True, amax=True), OracleRun(w, nq.rows_capacity(w.T, w.k, w.E, w.A)))
+    # routing edges: dropped slots, out-of-range and repeated ids add nothing
+    tokens = special_tokens()
+    T = tokens.shape[0]
+    topk = np.array([[i % 5, (i + 2) % 5] for i in range(T)], np.int32)
+    topk[1, 1] = -1
+    topk[2, 1] = 9
+    topk[3, 1] = topk[3, 0]
+    w = workloads.Workload("special", "special", tokens, topk, E=5)
+    for dispatch in (False, True):
+        g = GpuRun(w, dispatch=dispatch, amax=True)
+        compare_runs(g, OracleRun(w, g.R_cap))
+    # no tokens / one token (capacity below one tile: the receive reduces the
+    # trailers itself), empty experts (amax 0, S_enc 1)
+    for T, E in ((0, 4), (1, 1), (1, 8)):
+        rng = np.random.default_rng(T + E)
+        tokens = workloads.to_bf16_bits(rng.standard_normal((T, 256)).astype(np.float32))
+        k = min(2, E)
+        topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else \
+            np.zeros((0, k), np.int32)
+        w = workloads.Workload("edge", "edge", tokens, topk, E=E)
+        g = GpuRun(w, dispatch=True, amax=True)
+        compare_runs(g, OracleRun(w, g.R_cap))
+
+
+def test_parity_pack_reduced_amax_largest_and_wide():
+    """E = 1024, k = 32 (deepest search over the offsets in the separate
+    pack) and H = 16384 (the general pack kernel)."""
+    w = workloads.make(4, T=64, H=256, E=1024, k=32)
+    for dispatch in (False, True):
+        g = GpuRun(w, dispatch=dispatch, amax=True)
+        compare_runs(g, OracleRun(w, g.R_cap))
+    w = workloads.make(1, T=64, H=16384)
+    g = GpuRun(w, dispatch=True, amax=True)
+    compare_runs(g, OracleRun(w, g.R_cap))
+
+
+def test_pack_amax_accumulates_into_callers_values():
+    """ep_nvfp4_pack max-reduces into what the array holds: an entry above
+    every token amax stays, the others end at the experts' amax."""
+    w = workloads.make(2, T=300, H=512)
+    tok = to_dev_bf16(w.tokens)
+    plan = nq.ep_route_plan(torch.from_numpy(np.ascontiguousarray(w.topk)).cuda(), w.E, w.A)
+    amax = torch.zeros(w.E, dtype=torch.float32, device="cuda")
+    amax[1] = 1e30
+    nq.ep_nvfp4_pack(tok, plan, expert_amax=amax)
+    off, cnt, dest, _ = oracle.route_plan(w.topk, w.E, w.A)
+    rows = oracle.nvfp4_pack(w.tokens, dest, w.k, off, cnt, w.E, plan.R_cap)
+    want = oracle.nvfp4_direct_receive(rows, w.H, off, w.E)["amax_row"].copy()
+    want[1] = np.float32(1e30)
+    assert_bytes_equal(amax.cpu().numpy().view(np.uint32), want.view(np.uint32), "accumulated amax")
