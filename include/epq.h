@@ -174,9 +174,9 @@ ep_status ep_route_plan_noalloc(const int32_t *topk_idx, int64_t T, int k,
  *                   of reducing the row trailers itself.  The caller fills it
  *                   first (zeros, or the partial maxima of earlier packs into
  *                   the same rows).  4-byte aligned.  With it, the next kernel
- *                   on `stream` starts only after this call's kernel has
- *                   finished (no early start under programmatic dependent
- *                   launch).
+ *                   on `stream` may start (programmatic dependent launch) only
+ *                   as the pack's CTAs finish their work, not when they
+ *                   start.
  *   rounding        EP_ROUND_RNE or EP_ROUND_SR (element codes only; scales
  *                   are always round-to-nearest-even).  SR draws 8 bits per
  *                   element from Philox4x32-10 keyed by `seed`, counter

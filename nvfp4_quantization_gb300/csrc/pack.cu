@@ -254,11 +254,13 @@ nvfp4_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
 {
     __shared__ uint32_t wmax[2][kMaxThreads / 32];
     __shared__ float srcp[128];
-    if (!expert_amax)   // as in the warp kernel: a reader of the amax starts after this grid
+    if (!expert_amax)   // as in the warp kernel: a reader of the amax is let in as CTAs finish
         pdl_launch_dependents();
     pdl_wait();
     if ((int)blockIdx.x >= n_tok_ctas) {
         fill_padding(0, blockIdx.x - n_tok_ctas, pad_ctas, offsets, counts, E, R_cap, rows, S, H, status);
+        if (expert_amax)
+            pdl_launch_dependents();
         return;
     }
     for (int i = threadIdx.x; i < 128; i += blockDim.x)
@@ -369,6 +371,8 @@ nvfp4_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
                     w[c][i] = wn[c][i];
         }
     }
+    if (expert_amax)
+        pdl_launch_dependents();
 }
 
 // Encode NB blocks held by one lane (block b = lane + 32 b of the token).
@@ -446,13 +450,16 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
     __shared__ float srcp[128];
     __shared__ uint64_t bar[kPackWarps][kBuf];
     // With the per-expert amax reduced here, the next kernel (a direct receive
-    // that reads it) is let in only when this grid is done: started earlier,
-    // its CTAs would sit on the SMs this grid's last CTAs still need.
+    // that reads it) is let in only as this grid's CTAs finish their work (each
+    // triggers at its end): started earlier, its CTAs would sit on the SMs this
+    // grid's CTAs still need; it reads nothing before its wait on this grid.
     if (!expert_amax)
         pdl_launch_dependents();
     if ((int)blockIdx.x >= n_tok_ctas) {
         pdl_wait();
         fill_padding(0, blockIdx.x - n_tok_ctas, pad_ctas, offsets, counts, E, R_cap, rows, S, H, status);
+        if (expert_amax)
+            pdl_launch_dependents();
         return;
     }
     // Before the wait for the routing plan: pull this warp's first tokens
@@ -580,6 +587,8 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
                 red_max_nonneg(expert_amax + e, u2f(a_bits << 16));
         }
     }
+    if (expert_amax)
+        pdl_launch_dependents();
 }
 
 __global__ void __launch_bounds__(kMaxThreads)
