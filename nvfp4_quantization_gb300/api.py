@@ -188,12 +188,14 @@ def ep_nvfp4_unpack(rows: torch.Tensor, H: int, offsets: torch.Tensor, E: int,
 
 
 def alloc_grouped(R_cap: int, H: int, E: int, device, rowwise: bool = True) -> dict:
+    """Output tensors of the direct receive.  amax_row, amax_col and
+    cw_scale_enc are the three rows of one [3, E] tensor, ``metadata``, so a
+    single copy moves all three."""
     u8, f32 = torch.uint8, torch.float32
+    meta = torch.empty((3, E), dtype=f32, device=device)
     g = dict(cw_codes=torch.empty(R_cap * H // 2, dtype=u8, device=device),
              cw_scales=torch.empty(R_cap * H // 16, dtype=u8, device=device),
-             amax_row=torch.empty(E, dtype=f32, device=device),
-             amax_col=torch.empty(E, dtype=f32, device=device),
-             cw_scale_enc=torch.empty(E, dtype=f32, device=device))
+             amax_row=meta[0], amax_col=meta[1], cw_scale_enc=meta[2], metadata=meta)
     if rowwise:
         g.update(rw_codes=torch.empty((R_cap, H // 2), dtype=u8, device=device),
                  rw_scales=torch.empty((R_cap, H // 16), dtype=u8, device=device),
