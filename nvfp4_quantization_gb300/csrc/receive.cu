@@ -15,11 +15,14 @@
 // the tiles in row-major order, round robin, so the whole grid sweeps the
 // rows once, front to back.
 //
-// Two launches.  expert_amax_kernel reduces each expert's 4-byte token
-// amaxes from the row trailers (the rows' data is not read) into the expert's
-// metadata and encode scale S_enc.  The tile kernel, launched behind it with
-// programmatic dependent launch, starts its first tile loads while the amax
-// kernel runs and reads S_enc once per CTA after waiting for it.
+// Given the per-expert amax the pack reduced as it wrote the rows, one launch:
+// the tile kernel waits on the pack, issues its first tile loads, and derives
+// every expert's S_enc from the amax itself (CTA 0 writes the metadata).  From
+// the rows alone, two launches: expert_amax_kernel reduces each expert's
+// 4-byte token amaxes from the row trailers (the rows' data is not read) into
+// the expert's metadata and encode scale S_enc, and the tile kernel, launched
+// behind it with programmatic dependent launch, starts its first tile loads
+// while the amax kernel runs and reads S_enc once per CTA after waiting for it.
 //
 // Stages: a shared-memory ring of tiles (2 stages and 3 CTAs per SM for RNE,
 // 3 stages and 2 CTAs per SM for SR) loaded by 2-D TMA (codes 128 B
