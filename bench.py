@@ -164,15 +164,15 @@ def source_sha(paths) -> str:
 DR_SOURCES = ["nvfp4_quantization_gb300/csrc/receive.cu", "nvfp4_quantization_gb300/csrc/epq_device.cuh"]
 
 
-def profiled_traffic(kernel: str, sources) -> float | None:
+def profiled_traffic(kernel: str, sources, config: int) -> float | None:
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current kernel source and on this workload; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         rec = d[kernel]
-        if rec.get("source_sha") != source_sha(sources):
+        if rec.get("source_sha") != source_sha(sources) or rec.get("config") != config:
             return None
         return float(rec["dram_bytes_per_launch"])
     except Exception:
@@ -278,9 +278,7 @@ def gpu_arm(args, rank, world, local):
 
     # ---- timed region: K steps, rotating buffer sets (cold L2 per step).
     # Steps go in blocks of one step per set; one graph replay runs a whole
-    # block, so the host stays far ahead of the GPU.  Every SAMPLE_EVERY-th
-    # block is replayed kernel-group by kernel-group with CUDA events between
-    # them: those steps give the per-kernel durations of the roofline.
+    # block, so the host stays far ahead of the GPU.
     gR = capture_rotation(torch, sets)
     K, W = args.steps, args.warmup
     nset = len(sets)
@@ -290,9 +288,6 @@ def gpu_arm(args, rank, world, local):
     torch.cuda.synchronize()
     barrier()
     nblocks, rem = divmod(K, nset)
-    n_sampled = (nblocks + SAMPLE_EVERY - 1) // SAMPLE_EVERY
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(nset)] for _ in range(n_sampled)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     clocks.start()
@@ -300,16 +295,7 @@ def gpu_arm(args, rank, world, local):
     wall0 = time.perf_counter()
     t0.record()
     for blk in range(nblocks):
-        if blk % SAMPLE_EVERY == 0:
-            for j, b in enumerate(sets):
-                e = ev[blk // SAMPLE_EVERY][j]
-                e[0].record()
-                b.gA.replay()
-                e[1].record()
-                b.gB.replay()
-                e[2].record()
-        else:
-            gR.replay()
+        gR.replay()
     for j in range(rem):
         sets[j].gS.replay()
     t1.record()
@@ -319,6 +305,22 @@ def gpu_arm(args, rank, world, local):
     barrier()
     ms_total = max_over_ranks(dist, t0.elapsed_time(t1), "cuda")
     ms_step = ms_total / K
+    # ---- per-call durations for the roofline, after the timed region: one
+    # block in SAMPLE_EVERY again, each step replayed call by call with CUDA
+    # events between the calls (which stops the calls' overlap, so these steps
+    # are kept out of the step time)
+    n_sampled = max(1, (nblocks + SAMPLE_EVERY - 1) // SAMPLE_EVERY)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(nset)] for _ in range(n_sampled)]
+    for blk in range(n_sampled):
+        for j, b in enumerate(sets):
+            e = ev[blk][j]
+            e[0].record()
+            b.gA.replay()
+            e[1].record()
+            b.gB.replay()
+            e[2].record()
+    torch.cuda.synchronize()
     flat = [e for row in ev for e in row]
     ms_a = float(np.mean([e[0].elapsed_time(e[1]) for e in flat]))
     ms_b = float(np.mean([e[1].elapsed_time(e[2]) for e in flat]))
@@ -592,7 +594,7 @@ def main():
         "roofline": {"kernel": "direct_receive_kernel (ep_nvfp4_direct_receive)", "bound": "hbm",
                      "achieved": dr_gbs, "peak": peak, "unit": "GB/s", "frac": dr_gbs / peak,
                      "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": dr_b,
-                     "traffic": profiled_traffic("direct_receive", DR_SOURCES)},
+                     "traffic": profiled_traffic("direct_receive", DR_SOURCES, args.config)},
         "e2e": {"value": world * r["T"] / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"],
                 "api": "eager ep_nvfp4_dispatch / ep_nvfp4_direct_receive on two streams, "
