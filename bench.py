@@ -231,16 +231,18 @@ class BufferSet:
         torch.cuda.synchronize()
 
 
-def capture_rotation(torch, sets):
-    """One graph holding one step on every buffer set, in rotation order."""
+def capture_rotation(torch, sets, rotations: int = 1):
+    """One graph holding `rotations` rounds of one step on every buffer set,
+    in rotation order."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            for b in sets:
-                b.route_pack()
-                b.receive()
+            for _ in range(rotations):
+                for b in sets:
+                    b.route_pack()
+                    b.receive()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     return g
@@ -277,25 +279,32 @@ def gpu_arm(args, rank, world, local):
         b.capture(torch)
 
     # ---- timed region: K steps, rotating buffer sets (cold L2 per step).
-    # Steps go in blocks of one step per set; one graph replay runs a whole
-    # block, so the host stays far ahead of the GPU.
+    # Steps go in blocks of one step per set; whole blocks run as graphs of up
+    # to GRAPH_ROTATIONS blocks each (then single steps for a remainder), so
+    # the device runs them back to back with a launch gap only between graphs.
+    GRAPH_ROTATIONS = 50
     gR = capture_rotation(torch, sets)
     K, W = args.steps, args.warmup
     nset = len(sets)
     SAMPLE_EVERY = 10
+    nblocks, rem = divmod(K, nset)
+    n_big, n_small = divmod(nblocks, GRAPH_ROTATIONS)
+    gBig = capture_rotation(torch, sets, GRAPH_ROTATIONS) if n_big else None
+    gSmall = capture_rotation(torch, sets, n_small) if n_small else None
     for i in range(max(1, W // nset)):
         gR.replay()
     torch.cuda.synchronize()
     barrier()
-    nblocks, rem = divmod(K, nset)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     clocks.start()
     time.sleep(0.2)
     wall0 = time.perf_counter()
     t0.record()
-    for blk in range(nblocks):
-        gR.replay()
+    for _ in range(n_big):
+        gBig.replay()
+    if gSmall is not None:
+        gSmall.replay()
     for j in range(rem):
         sets[j].gS.replay()
     t1.record()
