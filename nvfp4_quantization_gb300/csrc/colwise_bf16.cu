@@ -56,8 +56,13 @@ __device__ __forceinline__ int cb_expert_of_row(const int *offs, int E, int row)
     return lo;
 }
 
+// Three CTAs per SM (at most 80 registers, no spills): the kernel is bound by
+// the loads it keeps in flight (16 words per lane, one unit ahead), so more
+// resident warps mean more bytes in flight (two CTAs per SM: 6 % slower).
+constexpr int kCbRhtCtasPerSm = 3;
+
 template <bool kSR>
-__global__ void __launch_bounds__(kCbThreads)
+__global__ void __launch_bounds__(kCbThreads, kCbRhtCtasPerSm)
 colwise_rht_bf16_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const int32_t *__restrict__ offsets,
                         int E, const float *__restrict__ amax_in, uint8_t *__restrict__ cw_codes,
                         uint8_t *__restrict__ cw_scales, float *__restrict__ amax_row, float *__restrict__ amax_col,
@@ -347,7 +352,7 @@ cudaError_t launch_colwise_rht_bf16(const LaunchCtx &c, const uint16_t *x, int R
     static const CbRcp rcp = make_cb_rcp();
     const int64_t units = (int64_t)(R_cap / 64) * (H / 16);
     int64_t grid = (units + (kCbThreads / 32) - 1) / (kCbThreads / 32);
-    const int64_t cap = (int64_t)c.num_sms * 4;
+    const int64_t cap = (int64_t)c.num_sms * kCbRhtCtasPerSm;   // one resident wave
     if (grid > cap)
         grid = cap;
     if (grid < 1)
