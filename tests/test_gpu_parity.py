@@ -68,6 +68,17 @@ def test_parity_swizzled_scales(name):
     compare_runs(g, o)
 
 
+def test_parity_swizzled_scales_256_row_slots():
+    """The tiled scale layout with expert slots aligned to 256 rows (A = 256):
+    every expert's columnwise scale matrix spans whole 128-row tile pairs, and
+    the rowwise matrix's tiles run across expert boundaries unchanged."""
+    w = workloads.make(2, T=700, H=1024)
+    w = workloads.Workload("a256", "a256", w.tokens, w.topk, E=w.E, A=256)
+    for dispatch in (False, True):
+        g = GpuRun(w, swizzled=True, dispatch=dispatch, amax=dispatch)
+        compare_runs(g, OracleRun(w, g.R_cap))
+
+
 def test_swizzled_scales_need_h_multiple_of_128():
     w = workloads.make(1, T=64, H=1056)
     tok = to_dev_bf16(w.tokens)
