@@ -27,7 +27,7 @@ def assert_bytes_equal(got: np.ndarray, want: np.ndarray, what: str):
                              f"got {got.reshape(-1)[i]!r} want {want.reshape(-1)[i]!r}")
 
 
-class GpuRun:
+class DeviceRun:
     """The hot path on the GPU for one workload, with canary-filled outputs."""
 
     def __init__(self, w, rowwise=True, mxfp8=False, unpack=False, R_cap=None, dispatch=False, swizzled=False,
@@ -94,7 +94,7 @@ class OracleRun:
         self.mx = oracle.mxfp8_pack(w.tokens, self.dest, w.k, self.off, self.cnt, w.E, R_cap) if mxfp8 else None
 
 
-def compare_runs(g: GpuRun, o: OracleRun, check_rowwise=True):
+def compare_runs(g: DeviceRun, o: OracleRun, check_rowwise=True):
     w = g.w
     H = w.H
     R = int(o.off[-1])

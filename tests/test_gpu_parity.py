@@ -10,7 +10,7 @@ import torch
 import nvfp4_quantization_gb300 as nq
 import oracle
 import workloads
-from paths import CANARY, GpuRun, OracleRun, assert_bytes_equal, compare_runs, to_dev_bf16
+from paths import CANARY, DeviceRun, OracleRun, assert_bytes_equal, compare_runs, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -30,7 +30,7 @@ CASES = {
 def test_parity_config(name):
     c = CASES[name]
     w = workloads.make(c["cfg"], **c["kw"])
-    g = GpuRun(w, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False))
+    g = DeviceRun(w, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False))
     o = OracleRun(w, g.R_cap, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False))
     compare_runs(g, o)
 
@@ -42,7 +42,7 @@ def test_parity_dispatch(name):
     ragged-H case takes the pack kernel without the early reads."""
     c = CASES[name]
     w = workloads.make(c["cfg"], **c["kw"])
-    g = GpuRun(w, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False), dispatch=True)
+    g = DeviceRun(w, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False), dispatch=True)
     o = OracleRun(w, g.R_cap, unpack=c.get("unpack", False), mxfp8=c.get("mxfp8", False))
     compare_runs(g, o)
 
@@ -51,7 +51,7 @@ def test_parity_dispatch_sr_many_tokens_per_warp():
     """More tokens than the pack's resident warps (several tokens per warp
     after the first), stochastic rounding, through ep_nvfp4_dispatch."""
     w = workloads.make(4, T=9000, H=512, E=32, k=3)
-    g = GpuRun(w, dispatch=True)
+    g = DeviceRun(w, dispatch=True)
     o = OracleRun(w, g.R_cap)
     compare_runs(g, o)
 
@@ -63,7 +63,7 @@ def test_parity_swizzled_scales(name):
     tiled layout (rowwise over rows [0, R), columnwise per expert)."""
     c = CASES[name]
     w = workloads.make(c["cfg"], **c["kw"])
-    g = GpuRun(w, swizzled=True)
+    g = DeviceRun(w, swizzled=True)
     o = OracleRun(w, g.R_cap)
     compare_runs(g, o)
 
@@ -75,7 +75,7 @@ def test_parity_swizzled_scales_256_row_slots():
     w = workloads.make(2, T=700, H=1024)
     w = workloads.Workload("a256", "a256", w.tokens, w.topk, E=w.E, A=256)
     for dispatch in (False, True):
-        g = GpuRun(w, swizzled=True, dispatch=dispatch, amax=dispatch)
+        g = DeviceRun(w, swizzled=True, dispatch=dispatch, amax=dispatch)
         compare_runs(g, OracleRun(w, g.R_cap))
 
 
@@ -93,14 +93,14 @@ def test_parity_rne_and_sr_on_same_tokens():
     base = workloads.make(4, T=200, H=512, E=16, k=4)
     for rounding, seed in ((0, 0), (1, 1), (1, 0xFFFFFFFFFFFF1234)):
         base.rounding, base.seed = rounding, seed
-        g = GpuRun(base)
+        g = DeviceRun(base)
         o = OracleRun(base, g.R_cap)
         compare_runs(g, o)
 
 
 def test_parity_without_rowwise_outputs():
     w = workloads.make(2, T=300, H=512)
-    g = GpuRun(w, rowwise=False)
+    g = DeviceRun(w, rowwise=False)
     o = OracleRun(w, g.R_cap)
     compare_runs(g, o, check_rowwise=False)
 
@@ -136,7 +136,7 @@ def test_parity_special_tokens_and_routing_edges():
     topk[2, 1] = 9            # id out of range -> status bit, dropped
     topk[3, 1] = topk[3, 0]   # repeated id -> status bit, later slot dropped
     w = workloads.Workload("special", "special", tokens, topk, E=5)
-    g = GpuRun(w, unpack=True, mxfp8=True)
+    g = DeviceRun(w, unpack=True, mxfp8=True)
     o = OracleRun(w, g.R_cap, unpack=True, mxfp8=True)
     assert o.status == 3
     compare_runs(g, o)
@@ -150,7 +150,7 @@ def test_parity_empty_and_single_token():
         topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else \
             np.zeros((0, k), np.int32)
         w = workloads.Workload("edge", "edge", tokens, topk, E=E)
-        g = GpuRun(w, unpack=True, mxfp8=True)
+        g = DeviceRun(w, unpack=True, mxfp8=True)
         o = OracleRun(w, g.R_cap, unpack=True, mxfp8=True)
         compare_runs(g, o)
 
@@ -160,12 +160,12 @@ def test_parity_all_slots_dropped_and_one_hot_expert():
     tokens = workloads.to_bf16_bits(rng.standard_normal((700, 256)).astype(np.float32))
     topk = np.full((700, 2), -1, np.int32)
     w = workloads.Workload("dropped", "dropped", tokens, topk, E=3)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     o = OracleRun(w, g.R_cap)
     compare_runs(g, o)
     topk = np.zeros((700, 1), np.int32) + 2   # every token to expert 2, 700 rows -> ragged 768
     w = workloads.Workload("hot", "hot", tokens, topk, E=3, A=256)
-    g = GpuRun(w, unpack=True)
+    g = DeviceRun(w, unpack=True)
     o = OracleRun(w, g.R_cap, unpack=True)
     compare_runs(g, o)
 
@@ -207,15 +207,15 @@ def test_parity_exhaustive_encode(kexp):
     topk = (np.arange(T, dtype=np.int32) % 4).reshape(T, 1)
     for rounding in (0, 1):
         w = workloads.Workload("exh", "exh", tokens, topk, E=4, rounding=rounding, seed=17)
-        g = GpuRun(w, unpack=True)
+        g = DeviceRun(w, unpack=True)
         o = OracleRun(w, g.R_cap, unpack=True)
         compare_runs(g, o)
 
 
 def test_deterministic_repeat():
     w = workloads.make(4, T=200, H=512, E=16, k=4)
-    a = GpuRun(w, mxfp8=True, unpack=True)
-    b = GpuRun(w, mxfp8=True, unpack=True)
+    a = DeviceRun(w, mxfp8=True, unpack=True)
+    b = DeviceRun(w, mxfp8=True, unpack=True)
     assert torch.equal(a.rows, b.rows)
     for k in a.grouped:
         assert torch.equal(a.grouped[k], b.grouped[k]), k
@@ -227,7 +227,7 @@ def test_cuda_graph_capture_matches_eager():
     the same bytes as the eager calls (the library allocates nothing and never
     synchronises, so every call is capturable)."""
     w = workloads.make(2, T=500, H=1024)
-    eager = GpuRun(w)
+    eager = DeviceRun(w)
     tok = to_dev_bf16(w.tokens)
     topk = torch.from_numpy(w.topk).cuda()
     R_cap = eager.R_cap
@@ -271,7 +271,7 @@ def test_device_guard_follows_input_device():
     current (single-GPU machines: the current device is set to a different
     value only if there is one)."""
     w = workloads.make(1, T=64, H=256)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     assert g.status == 0
     assert torch.cuda.current_device() == 0
 
@@ -438,7 +438,7 @@ def test_parity_largest_expert_count_and_slots():
     the general routing kernel, 1 024 mostly-padding slots, the direct
     receive's per-CTA expert tables at their full size."""
     w = workloads.make(4, T=64, H=256, E=1024, k=32)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     o = OracleRun(w, g.R_cap)
     compare_runs(g, o)
 
@@ -447,7 +447,7 @@ def test_parity_wide_hidden():
     """H = 16384: the pack's multi-chunk kernel (wider than the warp kernel's
     8192) and 64 column strips in the direct receive."""
     w = workloads.make(1, T=64, H=16384)
-    g = GpuRun(w, unpack=True, mxfp8=True)
+    g = DeviceRun(w, unpack=True, mxfp8=True)
     o = OracleRun(w, g.R_cap, unpack=True, mxfp8=True)
     compare_runs(g, o)
 
@@ -464,7 +464,7 @@ def test_parity_pack_reduced_amax(name, dispatch):
     cases take the general pack kernel."""
     c = CASES[name]
     w = workloads.make(c["cfg"], **c["kw"])
-    g = GpuRun(w, unpack=c.get("unpack", False), dispatch=dispatch, amax=True)
+    g = DeviceRun(w, unpack=c.get("unpack", False), dispatch=dispatch, amax=True)
     o = OracleRun(w, g.R_cap, unpack=c.get("unpack", False))
     compare_runs(g, o)
 
@@ -472,7 +472,7 @@ def test_parity_pack_reduced_amax(name, dispatch):
 def test_parity_pack_reduced_amax_swizzled_and_edges():
     # the tiled-scale receive with the supplied amax
     w = workloads.make(2, T=600, H=1024)
-    compare_runs(GpuRun(w, swizzled=True, dispatch=True, amax=True), OracleRun(w, nq.rows_capacity(w.T, w.k, w.E, w.A)))
+    compare_runs(DeviceRun(w, swizzled=True, dispatch=True, amax=True), OracleRun(w, nq.rows_capacity(w.T, w.k, w.E, w.A)))
     # routing edges: dropped slots, out-of-range and repeated ids add nothing
     tokens = special_tokens()
     T = tokens.shape[0]
@@ -482,7 +482,7 @@ def test_parity_pack_reduced_amax_swizzled_and_edges():
     topk[3, 1] = topk[3, 0]
     w = workloads.Workload("special", "special", tokens, topk, E=5)
     for dispatch in (False, True):
-        g = GpuRun(w, dispatch=dispatch, amax=True)
+        g = DeviceRun(w, dispatch=dispatch, amax=True)
         compare_runs(g, OracleRun(w, g.R_cap))
     # no tokens / one token (capacity below one tile: the receive reduces the
     # trailers itself), empty experts (amax 0, S_enc 1)
@@ -493,7 +493,7 @@ def test_parity_pack_reduced_amax_swizzled_and_edges():
         topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else \
             np.zeros((0, k), np.int32)
         w = workloads.Workload("edge", "edge", tokens, topk, E=E)
-        g = GpuRun(w, dispatch=True, amax=True)
+        g = DeviceRun(w, dispatch=True, amax=True)
         compare_runs(g, OracleRun(w, g.R_cap))
 
 
@@ -502,10 +502,10 @@ def test_parity_pack_reduced_amax_largest_and_wide():
     pack) and H = 16384 (the general pack kernel)."""
     w = workloads.make(4, T=64, H=256, E=1024, k=32)
     for dispatch in (False, True):
-        g = GpuRun(w, dispatch=dispatch, amax=True)
+        g = DeviceRun(w, dispatch=dispatch, amax=True)
         compare_runs(g, OracleRun(w, g.R_cap))
     w = workloads.make(1, T=64, H=16384)
-    g = GpuRun(w, dispatch=True, amax=True)
+    g = DeviceRun(w, dispatch=True, amax=True)
     compare_runs(g, OracleRun(w, g.R_cap))
 
 
