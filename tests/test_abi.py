@@ -115,6 +115,50 @@ def test_receive_and_unpack_validation():
     assert L.ep_nvfp4_unpack(None, 128, 1024, FAKE, 4, FAKE, FAKE, None) == -1
 
 
+def test_bf16_quantizer_validation():
+    L = nq.lib()
+    bad = ctypes.c_void_p(0x10008)    # 8-byte aligned only
+
+    def cw(**kw):
+        a = dict(x=FAKE, R=256, H=1024, off=FAKE, E=4, amax=FAKE, codes=FAKE, scales=FAKE, ar=FAKE, ac=FAKE,
+                 se=FAKE, rnd=0, st=FAKE)
+        a.update(kw)
+        return L.ep_nvfp4_colwise_rht_bf16(a["x"], a["R"], a["H"], a["off"], a["E"], a["amax"], a["codes"],
+                                           a["scales"], a["ar"], a["ac"], a["se"], a["rnd"], 0, 0, a["st"], None)
+    assert cw(amax=None) == -1 and cw(se=None) == -1 and cw(st=None) == -1
+    assert cw(H=1000) == -2 and cw(E=0) == -2 and cw(E=1025) == -2
+    assert cw(R=-1) == -4
+    assert cw(rnd=2) == -5
+    assert cw(x=bad) == -3 and cw(codes=bad) == -3
+
+    def mx(**kw):
+        a = dict(x=FAKE, R=256, H=1024, off=FAKE, E=4, buf=FAKE, st=FAKE)
+        a.update(kw)
+        return L.ep_mxfp8_colwise(a["x"], a["R"], a["H"], a["off"], a["E"], a["buf"], a["st"], None)
+    assert mx(buf=None) == -1 and mx(off=None) == -1
+    assert mx(H=48) == -2 and mx(E=0) == -2
+    assert mx(R=-1) == -4
+    assert mx(buf=bad) == -3
+
+
+def test_route_plan_noalloc_validation():
+    L = nq.lib()
+
+    def call(**kw):
+        a = dict(topk=FAKE, T=10, k=2, E=4, A=128, R=10 * 2 + 4 * 127, off=FAKE, cnt=FAKE, dest=FAKE, st=FAKE)
+        a.update(kw)
+        return L.ep_route_plan_noalloc(a["topk"], a["T"], a["k"], a["E"], a["A"], a["R"], a["off"], a["cnt"],
+                                       a["dest"], a["st"], None)
+    assert call(off=None) == -1 and call(st=None) == -1
+    assert call(k=0) == -2 and call(E=1025) == -2
+    assert call(A=64) == -3
+    assert call(R=10 * 2 + 4 * 127 - 1) == -4
+    # a plan larger than the fixed scratch is refused, not truncated
+    T, k, E = 1 << 20, 8, 1024
+    assert L.ep_route_workspace_bytes(T, k, E) > _lib.EP_ROUTE_STATIC_SCRATCH_BYTES
+    assert call(T=T, k=k, E=E, R=T * k + E * 127) == -4
+
+
 def test_static_scratch_size_matches_header():
     m = re.search(r"#define\s+EP_ROUTE_STATIC_SCRATCH_BYTES\s+(\d+)", open(HEADER).read())
     assert m and int(m.group(1)) == _lib.EP_ROUTE_STATIC_SCRATCH_BYTES
