@@ -259,8 +259,10 @@ typedef struct {
  *   expert_amax     device f32 [E] or NULL: each expert's amax, the largest
  *                   token amax A_t over its rows, already reduced (as
  *                   ep_nvfp4_pack / ep_nvfp4_dispatch leave it); the outputs
- *                   are then identical and no trailer pass is made.  NULL:
- *                   the call reduces the trailers itself.  4-byte aligned.
+ *                   are then identical and no trailer pass is made (below one
+ *                   128-row tile of capacity the trailers are read anyway, to
+ *                   the same result).  NULL: the call reduces the trailers
+ *                   itself.  4-byte aligned (EP_ERR_ALIGN otherwise).
  *   out             host pointer to the output descriptor.  The rowwise group
  *                   (rw_codes, rw_scales, rw_row_scale) may be all NULL to skip
  *                   it; everything else is required.
