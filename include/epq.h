@@ -178,9 +178,14 @@ ep_status ep_route_plan_noalloc(const int32_t *topk_idx, int64_t T, int k,
  *                   as the pack's CTAs finish their work, not when they
  *                   start.
  *   rounding        EP_ROUND_RNE or EP_ROUND_SR (element codes only; scales
- *                   are always round-to-nearest-even).  SR draws 8 bits per
- *                   element from Philox4x32-10 keyed by `seed`, counter
- *                   ((t*H + h)/16, 0, stream 0, 0).
+ *                   are always round-to-nearest-even).  SR gives element
+ *                   idx = t*H + h a 16-bit number R from Philox4x32-10 keyed
+ *                   by `seed`, counter (idx/16, idx/2^36, stream 0, 0): word
+ *                   (idx/4)%4 of the output, bytes b0..b3, A = b2:b0,
+ *                   B = b3:b1; idx%4 = 0, 1, 2, 3 takes A, A bit-reversed,
+ *                   B, B bit-reversed; the code rounds up iff
+ *                   R + 65536 f >= 65536 (f: position between the two
+ *                   neighbouring E2M1 values).
  * Numerics: A_t = max|x|; k = smallest integer >= -126 with A_t <= 2688*2^k;
  * s_b = E4M3_RNE(max|x_block| / (6*S_t)); code = E2M1(x / (s_b*S_t)), nearest
  * with ties to even, saturating at 6, sign kept (also for zero).

@@ -75,9 +75,9 @@ def _declare(L):
     L.or_e2m1_rne_batch.argtypes = [_P, _I64, _P]; L.or_e2m1_rne_batch.restype = None
     L.or_e2m1_sr_batch.argtypes = [_P, _P, _I64, _P]; L.or_e2m1_sr_batch.restype = None
     L.or_e4m3_rne_sat_batch.argtypes = [_P, _I64, _P]; L.or_e4m3_rne_sat_batch.restype = None
-    L.or_sr_bytes.argtypes = [_U64, ctypes.c_uint32, _U64, _I64, _P]; L.or_sr_bytes.restype = None
+    L.or_sr_u16s.argtypes = [_U64, ctypes.c_uint32, _U64, _I64, _P]; L.or_sr_u16s.restype = None
     L.or_philox4x32_10.argtypes = [_P, _P, _P]; L.or_philox4x32_10.restype = None
-    L.or_sr_byte.argtypes = [_U64, ctypes.c_uint32, _U64]; L.or_sr_byte.restype = ctypes.c_uint
+    L.or_sr_u16.argtypes = [_U64, ctypes.c_uint32, _U64]; L.or_sr_u16.restype = ctypes.c_uint
     L.or_rht16_f32.argtypes = [_P, _U16, _P]; L.or_rht16_f32.restype = None
     L.or_row_bytes.argtypes = [_I64]; L.or_row_bytes.restype = ctypes.c_size_t
     L.or_route_plan.argtypes = [_P, _I64, _I32, _I32, _I32, _P, _P, _P]
@@ -120,8 +120,8 @@ def e2m1_rne(v: float) -> int:
     return lib().or_e2m1_rne(float(v))
 
 
-def e2m1_sr(v: float, r8: int) -> int:
-    return lib().or_e2m1_sr(float(v), int(r8))
+def e2m1_sr(v: float, r16: int) -> int:
+    return lib().or_e2m1_sr(float(v), int(r16))
 
 
 def e4m3_value(code: int) -> float:
@@ -151,9 +151,9 @@ def e2m1_rne_batch(v) -> np.ndarray:
     return out
 
 
-def e2m1_sr_batch(v, r8) -> np.ndarray:
+def e2m1_sr_batch(v, r16) -> np.ndarray:
     v = _as(v, np.float64).reshape(-1)
-    r = _as(r8, np.uint8).reshape(-1)
+    r = _as(r16, np.uint16).reshape(-1)
     out = np.zeros(v.shape[0], np.uint8)
     lib().or_e2m1_sr_batch(_ptr(v), _ptr(r), v.shape[0], _ptr(out))
     return out
@@ -166,9 +166,10 @@ def e4m3_rne_sat_batch(v) -> np.ndarray:
     return out
 
 
-def sr_bytes(seed: int, stream: int, idx0: int, n: int) -> np.ndarray:
-    out = np.zeros(int(n), np.uint8)
-    lib().or_sr_bytes(int(seed), int(stream), int(idx0), int(n), _ptr(out))
+def sr_u16s(seed: int, stream: int, idx0: int, n: int) -> np.ndarray:
+    """The 16-bit random numbers of elements idx0 .. idx0+n-1 (reading R13)."""
+    out = np.zeros(int(n), np.uint16)
+    lib().or_sr_u16s(int(seed), int(stream), int(idx0), int(n), _ptr(out))
     return out
 
 
@@ -180,8 +181,8 @@ def philox4x32_10(ctr, key) -> np.ndarray:
     return out
 
 
-def sr_byte(seed: int, stream: int, idx: int) -> int:
-    return lib().or_sr_byte(int(seed), int(stream), int(idx))
+def sr_u16(seed: int, stream: int, idx: int) -> int:
+    return lib().or_sr_u16(int(seed), int(stream), int(idx))
 
 
 def rht16_f32(d, sign_mask: int = DEFAULT_SIGN_MASK) -> np.ndarray:

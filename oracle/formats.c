@@ -45,11 +45,13 @@ int or_e2m1_rne(double v)
     return sign | best;
 }
 
-/* Stochastic rounding to E2M1 with an 8-bit random number r8 (reading R13):
+/* Stochastic rounding to E2M1 with a 16-bit random number r16 (reading R13):
  * with lo <= |v| < hi the neighbouring grid values and f = (|v|-lo)/(hi-lo),
- * round up to hi iff r8 + floor(256 f) >= 256, i.e. with probability
- * floor(256 f)/256.  Grid values never move; |v| >= 6 gives 6.  Sign kept. */
-int or_e2m1_sr(double v, unsigned r8)
+ * round up to hi iff r16 + 65536 f >= 65536 (an exact comparison: 65536 f is
+ * exact in double), i.e. with probability floor(65536 f)/65536 over the
+ * 65536 values of r16.  Grid values never move; |v| >= 6 gives 6.  Sign
+ * kept. */
+int or_e2m1_sr(double v, unsigned r16)
 {
     int sign = signbit(v) ? 8 : 0;
     double a = fabs(v);
@@ -60,8 +62,7 @@ int or_e2m1_sr(double v, unsigned r8)
         ++i;
     double lo = kE2M1[i], hi = kE2M1[i + 1];
     double f = (a - lo) / (hi - lo);
-    double fl = floor(f * 256.0);
-    int up = ((double)(r8 & 255u) + fl) >= 256.0;
+    int up = ((double)(r16 & 0xffffu) + f * 65536.0) >= 65536.0;
     return sign | (up ? i + 1 : i);
 }
 
@@ -177,11 +178,24 @@ void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* The 8-bit random number of element idx in a given stream (reading R13): one
- * Philox call covers 16 consecutive elements.  Counter = (lo32(n), hi32(n),
- * stream, 0) with n = idx / 16, key = (lo32(seed), hi32(seed)); element idx
- * takes byte (idx mod 4) of output word ((idx / 4) mod 4), little-endian. */
-unsigned or_sr_byte(uint64_t seed, uint32_t stream, uint64_t idx)
+/* The 16 bits of x in reverse order (bit 0 <-> bit 15). */
+static unsigned reverse16(unsigned x)
+{
+    unsigned r = 0;
+    for (int b = 0; b < 16; ++b)
+        if (x & (1u << b))
+            r |= 1u << (15 - b);
+    return r;
+}
+
+/* The 16-bit random number of element idx in a given stream (reading R13).
+ * One Philox call covers 16 consecutive elements: counter = (lo32(n),
+ * hi32(n), stream, 0) with n = idx / 16, key = (lo32(seed), hi32(seed)).
+ * Element idx uses output word q = (idx / 4) mod 4; with b0..b3 the bytes of
+ * that word (b0 the least significant), A = b2 * 256 + b0 and
+ * B = b3 * 256 + b1, the four elements of the word take, for j = idx mod 4:
+ * j = 0: A, j = 1: A bit-reversed, j = 2: B, j = 3: B bit-reversed. */
+unsigned or_sr_u16(uint64_t seed, uint32_t stream, uint64_t idx)
 {
     uint64_t n = idx / 16;
     uint32_t ctr[4] = {(uint32_t)n, (uint32_t)(n >> 32), stream, 0u};
@@ -189,7 +203,14 @@ unsigned or_sr_byte(uint64_t seed, uint32_t stream, uint64_t idx)
     uint32_t out[4];
     or_philox4x32_10(ctr, key, out);
     uint32_t w = out[(idx / 4) % 4];
-    return (w >> (8 * (idx % 4))) & 0xffu;
+    unsigned b0 = w & 0xffu, b1 = (w >> 8) & 0xffu, b2 = (w >> 16) & 0xffu, b3 = w >> 24;
+    unsigned A = (b2 << 8) | b0, B = (b3 << 8) | b1;
+    switch (idx % 4) {
+    case 0: return A;
+    case 1: return reverse16(A);
+    case 2: return B;
+    default: return reverse16(B);
+    }
 }
 
 /* 16-point random Hadamard transform (reading R9): u_i = sigma_i * d_i / 4,
@@ -227,10 +248,10 @@ void or_e2m1_rne_batch(const double *v, int64_t n, uint8_t *out)
         out[i] = (uint8_t)or_e2m1_rne(v[i]);
 }
 
-void or_e2m1_sr_batch(const double *v, const uint8_t *r8, int64_t n, uint8_t *out)
+void or_e2m1_sr_batch(const double *v, const uint16_t *r16, int64_t n, uint8_t *out)
 {
     for (int64_t i = 0; i < n; ++i)
-        out[i] = (uint8_t)or_e2m1_sr(v[i], r8[i]);
+        out[i] = (uint8_t)or_e2m1_sr(v[i], r16[i]);
 }
 
 void or_e4m3_rne_sat_batch(const double *v, int64_t n, uint8_t *out)
@@ -239,8 +260,8 @@ void or_e4m3_rne_sat_batch(const double *v, int64_t n, uint8_t *out)
         out[i] = (uint8_t)or_e4m3_rne_sat(v[i]);
 }
 
-void or_sr_bytes(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t n, uint8_t *out)
+void or_sr_u16s(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t n, uint16_t *out)
 {
     for (int64_t i = 0; i < n; ++i)
-        out[i] = (uint8_t)or_sr_byte(seed, stream, idx0 + (uint64_t)i);
+        out[i] = (uint16_t)or_sr_u16(seed, stream, idx0 + (uint64_t)i);
 }

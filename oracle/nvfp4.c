@@ -64,7 +64,7 @@ void or_nvfp4_pack_token(const uint16_t *x, int64_t H, uint32_t token_id,
             } else {
                 double v = xv / s;
                 if (rounding == 1)
-                    code = or_e2m1_sr(v, or_sr_byte(seed, 0u, t_index * (uint64_t)H + (uint64_t)h));
+                    code = or_e2m1_sr(v, or_sr_u16(seed, 0u, t_index * (uint64_t)H + (uint64_t)h));
                 else
                     code = or_e2m1_rne(v);
             }

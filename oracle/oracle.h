@@ -44,7 +44,7 @@ extern "C" {
 /* ---- number formats ------------------------------------------------------ */
 double   or_e2m1_value(int code);                  /* 4-bit code -> value           */
 int      or_e2m1_rne(double v);                    /* nearest, ties to even index   */
-int      or_e2m1_sr(double v, unsigned r8);        /* stochastic, 8 random bits     */
+int      or_e2m1_sr(double v, unsigned r16);       /* stochastic, 16 random bits    */
 double   or_e4m3_value(int code);                  /* 8-bit code -> value (NaN: 0x7f/0xff) */
 int      or_e4m3_rne_sat(double v);                /* nearest, ties even, saturating */
 double   or_bf16_value(uint16_t bits);
@@ -52,13 +52,13 @@ uint16_t or_bf16_rne(double v);                    /* exact for |v| >= 2^-149 wi
 int      or_token_scale_exp(double amax);          /* k_t of the power-of-two token scale */
 int      or_mx_scale_exp(double bmax);             /* E8M0 exponent of an MXFP8 block */
 void     or_e2m1_rne_batch(const double *v, int64_t n, uint8_t *out);
-void     or_e2m1_sr_batch(const double *v, const uint8_t *r8, int64_t n, uint8_t *out);
+void     or_e2m1_sr_batch(const double *v, const uint16_t *r16, int64_t n, uint8_t *out);
 void     or_e4m3_rne_sat_batch(const double *v, int64_t n, uint8_t *out);
 
 /* ---- counter-based random numbers ---------------------------------------- */
 void     or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
-unsigned or_sr_byte(uint64_t seed, uint32_t stream, uint64_t idx);
-void     or_sr_bytes(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t n, uint8_t *out);
+unsigned or_sr_u16(uint64_t seed, uint32_t stream, uint64_t idx);
+void     or_sr_u16s(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t n, uint16_t *out);
 
 /* ---- 16-point random Hadamard transform along tokens ------------------- */
 void     or_rht16_f32(const float d[16], uint16_t sign_mask, float y[16]);

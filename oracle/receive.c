@@ -136,7 +136,7 @@ void or_nvfp4_direct_receive(const uint8_t *rows, int64_t R_cap, int64_t H,
                     int64_t pos = 16 * j + i; /* row within the expert */
                     int code;
                     if (rounding == 1)
-                        code = or_e2m1_sr(sv, or_sr_byte(seed, 1u,
+                        code = or_e2m1_sr(sv, or_sr_u16(seed, 1u,
                                    (uint64_t)off * (uint64_t)H + (uint64_t)h * (uint64_t)n + (uint64_t)pos));
                     else
                         code = or_e2m1_rne(sv);
@@ -254,7 +254,7 @@ void or_nvfp4_colwise_rht_bf16(const uint16_t *x, int64_t R_cap, int64_t H,
                     int64_t pos = 16 * j + i; /* row within the expert */
                     int code;
                     if (rounding == 1)
-                        code = or_e2m1_sr(sv, or_sr_byte(seed, 2u,
+                        code = or_e2m1_sr(sv, or_sr_u16(seed, 2u,
                                    (uint64_t)off * (uint64_t)H + (uint64_t)h * (uint64_t)n + (uint64_t)pos));
                     else
                         code = or_e2m1_rne(sv);
