@@ -186,7 +186,7 @@ colwise_rht_bf16_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const 
             u[i] = mul2(u[i], r2);
         uint2 c0, c1;
         if (kSR) {
-            // row i of the block takes random byte i of its column's 16 bytes (stream 2)
+            // rows 4q .. 4q + 3 of the block take word q of its column's Philox output (stream 2)
             const uint64_t pos = (uint64_t)off * (uint64_t)H + (uint64_t)h0 * (uint64_t)n + (uint64_t)(rl + 16 * j);
             const Philox4 ra = sr_bytes16(key, 2u, pos);
             const Philox4 rb = sr_bytes16(key, 2u, pos + (uint64_t)n);

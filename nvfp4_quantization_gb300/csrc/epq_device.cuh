@@ -426,9 +426,10 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
     return Philox4{c0, c1, c2, c3};
 }
 
-// The 16 random bytes of the aligned group of 16 elements starting at element
-// index idx0 (idx0 % 16 == 0) of stream `stream`: byte i of the result (word
-// i/4, byte i%4, little-endian) belongs to element idx0 + i.
+// The Philox output for the aligned group of 16 elements starting at element
+// index idx0 (idx0 % 16 == 0) of stream `stream`: word q (x, y, z, w for
+// q = 0..3) carries the random numbers of elements idx0 + 4q .. idx0 + 4q + 3
+// (see cvt_e2m1x8_sr).
 __device__ __forceinline__ Philox4 sr_bytes16(const PhiloxKey &K, uint32_t stream, uint64_t idx0)
 {
     const uint64_t n = idx0 >> 4;
@@ -436,74 +437,31 @@ __device__ __forceinline__ Philox4 sr_bytes16(const PhiloxKey &K, uint32_t strea
 }
 
 // Eight FP32 values -> one word of eight E2M1 codes by stochastic rounding,
-// a[0] in the lowest nibble; element i takes random byte i of (r_lo, r_hi)
-// (r_lo bytes 0..3 for a[0..3], r_hi for a[4..7]).  The rule is that of
-// sr_e2m1_value below: with lo <= |v| < hi the neighbouring grid values, round
-// up iff r + floor(256 (|v| - lo) / (hi - lo)) >= 256; sign kept, saturating.
+// a[0] in the lowest nibble; a[0..3] take the random word r_lo, a[4..7] r_hi.
+// Within a word with bytes b0..b3 (b0 least significant), A = b2:b0 and
+// B = b3:b1 (16-bit numbers, high byte first): the four values take A, A
+// bit-reversed, B, B bit-reversed; a value rounds up iff R + 65536 f >= 65536
+// with f its position between the neighbouring grid values, sign kept,
+// saturating at 6.
 //
-// Hardware: cvt.rs.satfinite.e2m1x4.f32 rounds its four operands with a
-// random number per operand taken from its 32-bit rbits operand.  Measured on
-// GB300 (an exhaustive check of single-bit and random rbits words): operands 1
-// and 3 use the 16-bit numbers rbits[31:24]:rbits[15:8] and
-// rbits[23:16]:rbits[7:0] (weight 2^-16 per unit; operands 0 and 2 use the
-// same two numbers bit-reversed), rounding up iff |fraction| + R >= 1.  With
-// rbits[15:0] = 0 this is exactly the 8-bit rule above for operands 1 and 3,
-// so each conversion here carries two values, in operands 1 and 3.
-//
-// Pairing: conversion j takes elements (j', j' + 2) of a group of four in
-// operands 3 and 1 (random bytes j' and j' + 2 moved to rbits[23:16] and
-// rbits[31:24] by one byte permute with zero), so the four 16-bit results
-// packed as (even elements | odd elements << 4) are the final word.
+// Hardware: cvt.rs.satfinite.e2m1x4.f32 d, {a, b, c, e}, rbits puts e in bits
+// 3:0 of d, c in 7:4, b in 11:8, a in 15:12, and rounds e with the 16-bit
+// number rbits[23:16]:rbits[7:0], b with rbits[31:24]:rbits[15:8], c and a
+// with the bit reverses of those two; a value rounds up iff its fraction plus
+// R 2^-16 reaches 1 (measured on GB300 over 8.4 M values with random words
+// and boundary fractions: 0 mismatches).  So the rule above is exactly one
+// conversion per four values with the Philox word as rbits.
 __device__ __forceinline__ uint32_t cvt_e2m1x8_sr(float a0, float a1, float a2, float a3, float a4, float a5,
                                                   float a6, float a7, uint32_t r_lo, uint32_t r_hi)
 {
     uint32_t out;
-    asm("{\n\t.reg .b16 h0, h1, h2, h3;\n\t"
-        ".reg .b32 q0, q1, q2, q3, e, o;\n\t"
-        "prmt.b32 q0, %9, 0, 0x2044;\n\t"
-        "prmt.b32 q1, %9, 0, 0x3144;\n\t"
-        "prmt.b32 q2, %10, 0, 0x2044;\n\t"
-        "prmt.b32 q3, %10, 0, 0x3144;\n\t"
-        "cvt.rs.satfinite.e2m1x4.f32 h0, {%11, %3, %11, %1}, q0;\n\t"
-        "cvt.rs.satfinite.e2m1x4.f32 h1, {%11, %4, %11, %2}, q1;\n\t"
-        "cvt.rs.satfinite.e2m1x4.f32 h2, {%11, %7, %11, %5}, q2;\n\t"
-        "cvt.rs.satfinite.e2m1x4.f32 h3, {%11, %8, %11, %6}, q3;\n\t"
-        "mov.b32 e, {h0, h2};\n\t"
-        "mov.b32 o, {h1, h3};\n\t"
-        "shl.b32 o, o, 4;\n\t"
-        "or.b32 %0, e, o;\n\t}"
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h0, {%4, %3, %2, %1}, %9;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h1, {%8, %7, %6, %5}, %10;\n\t"
+        "mov.b32 %0, {h0, h1};\n\t}"
         : "=r"(out)
-        : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7), "r"(r_lo), "r"(r_hi),
-          "f"(0.0f));
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7), "r"(r_lo), "r"(r_hi));
     return out;
-}
-
-// Stochastic rounding of an FP32 value onto the E2M1 grid with an 8-bit random
-// number r (0..255): with lo <= |v| < hi the neighbouring grid values, the
-// result is hi iff r + floor(256 (|v| - lo) / (hi - lo)) >= 256.  Returns the
-// grid value (exactly representable) with the sign of v; values >= 6 in
-// magnitude are returned as is (the saturating E2M1 conversion maps them to
-// +-6).  On [1, 6) the grid keeps one mantissa bit, so adding r below that bit
-// and truncating carries with exactly that probability; on [0, 1) the same is
-// done on 1 + |v| (added toward zero, so the fraction bits are the floor of
-// |v| * 2^23) where the grid step is 0.5 = one mantissa bit of [1, 2).
-__device__ __forceinline__ float sr_e2m1_value(float v, uint32_t r)
-{
-    uint32_t bits = f2u(v);
-    uint32_t sign = bits & 0x80000000u;
-    float a = u2f(bits & 0x7fffffffu);
-    uint32_t radd = r << 14;
-    float out;
-    if (a >= 6.0f) {
-        out = a;
-    } else if (a >= 1.0f) {
-        out = u2f((f2u(a) + radd) & 0xffc00000u);
-    } else {
-        uint32_t z = f2u(__fadd_rz(a, 1.0f));
-        uint32_t idx = ((z + radd) >> 22) - 254u; // 0, 1 or 2
-        out = (float)idx * 0.5f;
-    }
-    return u2f(f2u(out) | sign);
 }
 
 } // namespace epq

@@ -121,7 +121,7 @@ __device__ __forceinline__ uint2 encode_block16(const uint32_t *w, float s, floa
         v[2 * i] = q.x;
         v[2 * i + 1] = q.y;
     }
-    if (kSR) // element i takes random byte i % 4 of rnd[i / 4]
+    if (kSR) // elements 4q .. 4q + 3 take the random word rnd[q]
         return make_uint2(cvt_e2m1x8_sr(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], rnd[0], rnd[1]) ^ 0x88888888u,
                           cvt_e2m1x8_sr(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15], rnd[2], rnd[3]) ^
                               0x88888888u);

@@ -333,7 +333,7 @@ __device__ __forceinline__ void rht_block(const Sm &sm, int s, const void *tab, 
     for (int i = 0; i < 16; ++i)
         u[i] = mul2(u[i], r2);
     if (kSR) {
-        // row i of the block takes random byte i of its column's 16 bytes
+        // rows 4q .. 4q + 3 of the block take word q of its column's Philox output
         const uint64_t pos = (uint64_t)m.off * (uint64_t)p.H + (uint64_t)h0 * (uint64_t)m.n + (uint64_t)(rl + r0);
         const Philox4 ra = sr_bytes16(p.key, 1u, pos);
         const Philox4 rb = sr_bytes16(p.key, 1u, pos + (uint64_t)m.n);
