@@ -135,9 +135,12 @@ ep_status ep_route_plan(const int32_t *topk_idx, int64_t T, int k, int E, int A,
  *   Memory: allocates nothing, on any call.  The scratch is a fixed device
  *   array of EP_ROUTE_STATIC_SCRATCH_BYTES that every GPU which loads the
  *   library holds until the process exits.  The first call on a device looks
- *   up that device's scratch address (cudaGetSymbolAddress); make that first
- *   call before any stream capture on the device.  Each call clears the
- *   scratch's barrier words on `stream` before its kernel.
+ *   up that device's scratch address (cudaGetSymbolAddress), and so does the
+ *   first call after the device's context was replaced (e.g. by
+ *   cudaDeviceReset); make those calls before any stream capture: one made
+ *   while `stream` is capturing returns EP_ERR_ARG and enqueues nothing.
+ *   Each call clears the scratch's barrier words on `stream` before its
+ *   kernel.
  *   Concurrency: all calls on a device share one scratch array, so calls
  *   whose work may overlap on the GPU (different streams, or several host
  *   threads) race and give wrong plans; order them on one stream, or use

@@ -13,6 +13,7 @@
 // library holds its EP_ROUTE_STATIC_SCRATCH_BYTES until the process exits,
 // and every call on a device shares that device's copy, so two calls whose
 // kernels overlap on one GPU (two streams, or two host threads) race on it.
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -33,22 +34,62 @@ static __device__ __align__(256) uint32_t g_route_scratch[EP_ROUTE_STATIC_SCRATC
 
 // In host code `g_route_scratch` names a host-side stand-in, not device
 // memory: only the address cudaGetSymbolAddress returns (per device, with
-// that device current) may be handed to a kernel.
+// that device current) may be handed to a kernel.  The address belongs to the
+// device's current context: after that context is destroyed and a new one
+// made (cudaDeviceReset, for one), the module is loaded again, possibly
+// elsewhere.  So each cached address carries the unique id of the context it
+// was looked up in, and a different current context looks it up again.
 std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
 
-cudaError_t scratch_address(int dev, void **out)
+// Unique id of the calling thread's current context (driver entry points,
+// found through the runtime so that nothing links libcuda directly).
+cudaError_t current_context_id(unsigned long long *id)
+{
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    if (!get_current || !get_id) {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &r1) != cudaSuccess ||
+            r1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) != cudaSuccess ||
+            r2 != cudaDriverEntryPointSuccess)
+            return cudaErrorNotSupported;
+        get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(q);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, id) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
+
+// The scratch address of device `dev` (current) in its current context.  The
+// look-up is set-up work that must not run inside a stream capture: if the
+// address is not known yet for this context and `stream` is capturing, the
+// call fails (EP_ERR_ARG) instead.
+ep_status scratch_address(int dev, cudaStream_t stream, void **out)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != cudaSuccess)
+        return EP_ERR_CUDA;
+    if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess)
+            return EP_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone)
+            return EP_ERR_ARG;
         void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
-        if (e != cudaSuccess)
-            return e;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess)
+            return EP_ERR_CUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
-    return cudaSuccess;
+    return EP_OK;
 }
 
 int owning_device(const void *p)
@@ -98,9 +139,14 @@ extern "C" ep_status ep_route_plan_noalloc(const int32_t *topk_idx, int64_t T, i
     }
     void *scratch = nullptr;
     int nsm = 0;
-    cudaError_t e = scratch_address(dev, &scratch);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const ep_status se = scratch_address(dev, (cudaStream_t)stream, &scratch);
+    if (se != EP_OK) {
+        (void)cudaGetLastError();
+        if (prev != dev)
+            cudaSetDevice(prev);
+        return se;
+    }
+    cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = cudaMemsetAsync(scratch, 0, 16, (cudaStream_t)stream);   // barrier count and generation
     if (e == cudaSuccess) {

@@ -3,10 +3,10 @@
 It exists for callers that cannot allocate device memory for a workspace (a
 runtime that owns the whole GPU's memory in its own pool, a loop where a
 cudaMalloc would stall the device): it keeps its scratch in a fixed array
-inside the library instead.  Its plan must be identical, byte for byte, to
-ep_route_plan's on the same inputs -- routing is integer work -- including on
-consecutive calls, where the scratch still holds the previous call's totals
-and barrier words.
+inside the library instead.  Its plan must be identical, byte for byte, to the
+oracle's plan and to ep_route_plan's on the same inputs -- routing is integer
+work -- including on consecutive calls, where the scratch still holds the
+previous call's totals and barrier words.
 
 The file is named so that pytest collects it last: a run that stops at the
 first failure has run every other test before this one.  Outputs are
@@ -20,6 +20,7 @@ import pytest
 import torch
 
 import nvfp4_quantization_gb300 as nq
+import oracle
 from nvfp4_quantization_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
@@ -52,14 +53,21 @@ def _noalloc_plan(topk, E, A=128):
 
 
 def _same_plan(topk, E, got):
+    """The no-alloc plan equals the oracle's plan of the same routing (the
+    definition), and ep_route_plan's (the library's other entry point)."""
     ref = nq.ep_route_plan(topk, E, 128)
     torch.cuda.synchronize()
     off, cnt, dest, st = got
     T, k = topk.shape
+    o_off, o_cnt, o_dest, o_st = oracle.route_plan(topk.cpu().numpy(), E, 128)
+    assert np.array_equal(off.cpu().numpy(), o_off)
+    assert np.array_equal(cnt.cpu().numpy(), o_cnt)
+    assert np.array_equal(dest[: T * k].cpu().numpy(), o_dest[: T * k])
+    assert int(st.item()) == int(o_st) == 0
     assert torch.equal(off.cpu(), ref.offsets.cpu())
     assert torch.equal(cnt.cpu(), ref.counts.cpu())
     assert torch.equal(dest[: T * k].cpu(), ref.dest[: T * k].cpu())
-    assert int(st.item()) == int(ref.status.item()) == 0
+    assert int(ref.status.item()) == 0
 
 
 # (T, E, k): the register fast path at the 16K-token, 256-expert top-8 size;
