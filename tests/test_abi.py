@@ -49,6 +49,25 @@ def test_status_strings():
         assert _lib.status_string(s).startswith("EP_")
 
 
+def test_host_memory_is_refused_with_ep_err_device():
+    """Device guard, host side: pointers that are not device memory of the
+    input's device (here plain host memory, which also holds on a machine
+    without a GPU) return EP_ERR_DEVICE once the sizes are valid."""
+    import numpy as np
+    L = nq.lib()
+    buf = np.zeros(1 << 20, np.int32)
+    h = ctypes.c_void_p(buf.ctypes.data)
+    T, k, E = 10, 2, 4
+    R_cap = T * k + E * 127
+    assert L.ep_route_plan(h, T, k, E, 128, R_cap, h, h, h, h, 1 << 20, h, None) == -6
+    assert L.ep_nvfp4_pack(h, T, 1024, h, k, h, h, E, h, R_cap, None, 0, 0, h, None) == -6
+    assert L.ep_nvfp4_unpack(h, R_cap, 1024, h, E, h, h, None) == -6
+    g = _lib.EpGrouped(cw_codes=h.value, cw_scales=h.value, amax_row=h.value, amax_col=h.value, cw_scale_enc=h.value)
+    assert L.ep_nvfp4_direct_receive(h, R_cap, 1024, h, E, None, ctypes.byref(g), 0, 0, 0, h, None) == -6
+    assert L.ep_mxfp8_pack(h, T, 1024, h, k, h, h, E, h, R_cap, h, None) == -6
+    assert buf.sum() == 0     # nothing was written
+
+
 def test_route_plan_validation():
     L = nq.lib()
     f = L.ep_route_plan

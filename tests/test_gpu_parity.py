@@ -266,14 +266,34 @@ def test_cuda_graph_capture_matches_eager():
             assert torch.equal(v, ref), k
 
 
-def test_device_guard_follows_input_device():
-    """The call runs on the device of its input even when another device is
-    current (single-GPU machines: the current device is set to a different
-    value only if there is one)."""
-    w = workloads.make(1, T=64, H=256)
-    g = DeviceRun(w)
-    assert g.status == 0
-    assert torch.cuda.current_device() == 0
+def test_pointer_off_the_input_device_is_refused():
+    """Device guard: every pointer must be memory of the device that owns the
+    first input.  A call whose output lives in host memory (pinned, so that
+    CUDA knows it) returns EP_ERR_DEVICE and enqueues nothing: the device
+    outputs it was also given keep their contents."""
+    import ctypes
+    from nvfp4_quantization_gb300 import _lib
+    T, k, E = 64, 2, 4
+    topk = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    topk[:, 1] = 1
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((E,), -7, dtype=torch.int32, device="cuda")
+    dest_host = torch.full((T * k,), -7, dtype=torch.int32).pin_memory()
+    ws = nq.new_route_workspace(T, k, E, "cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    R_cap = nq.rows_capacity(T, k, E, 128)
+    s = _lib.lib().ep_route_plan(p(topk), T, k, E, 128, R_cap, p(off), p(cnt), p(dest_host), p(ws),
+                                 ws.numel() * 4, p(st), None)
+    torch.cuda.synchronize()
+    assert s == -6                                    # EP_ERR_DEVICE
+    assert torch.all(off == -7) and torch.all(cnt == -7) and torch.all(dest_host == -7)
+    # the same call with the destination on the device runs
+    dest = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+    s = _lib.lib().ep_route_plan(p(topk), T, k, E, 128, R_cap, p(off), p(cnt), p(dest), p(ws), ws.numel() * 4,
+                                 p(st), None)
+    torch.cuda.synchronize()
+    assert s == 0 and int(off[E].item()) == 2 * 128
 
 
 @pytest.mark.parametrize("T,E,k", [(3000, 32, 12), (400000, 64, 2), (20000, 1024, 3)])
