@@ -1,19 +1,25 @@
 """Benchmark of the NVFP4 EP hot path: route plan + NVFP4 pack + direct receive.
 
-Workload: 4096 tokens x 4096 hidden BF16 ~N(0,1) with 0.1% of entries x50;
-16 experts, softmax-of-Gaussian top-2 routing with 2 experts forced empty;
-alignment 128; round-to-nearest-even (the dispatch-forward configuration).
-A step is one pass of the whole path over one batch: route plan (1 kernel),
-NVFP4 pack with the routing gather (1 kernel), direct receive (2 kernels:
-per-expert amax from the row trailers, then the tiled rowwise /
-columnwise-RHT transform).
+Headline workload (the largest configuration): combine-backward gradients,
+16384 tokens x 7168 hidden BF16 ~ 1e-3 N(0,1) lognormal(0,1) per token;
+256 experts, top-8 uniform routing with 26 experts empty; alignment 128;
+stochastic rounding (Philox seed 1234) in the pack and the columnwise
+requantisation.  A step is one pass of the whole path over one batch: route
+plan (1 kernel) and NVFP4 pack with the routing gather (1 kernel, which also
+reduces the per-expert amax) in one ep_nvfp4_dispatch call, then the direct
+receive given that amax (1 kernel: the tiled rowwise / columnwise-RHT
+transform).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--config 1..5]
+                  [--config 1..5] [--no-extra-configs]
 
-``--config`` picks another of the five synthetic workloads (the same step:
-route plan + NVFP4 pack + direct receive; config 5's MXFP8 pack is not part
-of it); the default is the dispatch-forward batch above.
+``--config`` picks another of the five synthetic workloads for the headline
+(the same step).  With the default headline the line also carries, as nested
+keys: ``configs`` -- the dispatch-forward (4096x4096) and imbalanced
+(8192x4096) batches timed the same way, each with its own roofline block --
+and ``config5`` -- the MXFP8 vs NVFP4 comparison on the StudentT(4) batch:
+both packs timed, the NVFP4 step timed, and the relative RMS decode error of
+each format computed from the GPU outputs.
 
 Prints one JSON line (rank 0).  Under torchrun every rank processes its own
 batch (replicas: the path shards by token batch with no exchange on one
@@ -41,24 +47,28 @@ if ROOT not in sys.path:
 
 METRIC = "NVFP4 pack+direct-receive tokens/s and achieved HBM GB/s vs GB300 peak"
 UNIT = "tokens/s"
-WORKLOAD_CFG = 2          # the dispatch-forward config the metric is quoted on
+WORKLOAD_CFG = 4          # the largest configuration (16384x7168, 256 experts top-8, SR)
+EXTRA_CONFIGS = (2, 3)    # the other pack + direct-receive batches, nested in the same line
 KERNELS_PER_STEP = 3      # route plan, pack (reducing the per-expert amax), direct receive tile transform
-N_SETS = 6                # rotating buffer sets: ~560 MB touched per rotation > 129 MB L2
+L2_BYTES = 129 << 20
 FALLBACK_HBM_GBS = 6800.0
+DEFAULT_SEEDS = {1: 0, 2: 2, 3: 3, 4: 4, 5: 5}   # each workload's own seed
 
 
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (0: sized to about a second)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
-    p.add_argument("--sets", type=int, default=N_SETS, help="rotating buffer sets (profiling uses 1)")
+    p.add_argument("--no-extra-configs", action="store_true",
+                   help="only the headline workload (no nested configs 2, 3 and the config-5 comparison)")
+    p.add_argument("--sets", type=int, default=0, help="rotating buffer sets (0: enough to exceed the L2)")
     p.add_argument("--config", type=int, default=WORKLOAD_CFG, choices=[1, 2, 3, 4, 5],
-                   help="workload (default: the 4096-token dispatch-forward batch the metric is quoted on)")
+                   help="headline workload (default: the largest, the 16384x7168 SR combine-backward batch)")
     return p.parse_args()
 
 
@@ -69,10 +79,10 @@ def dist_env():
     return rank, world, local
 
 
-def replica_workload_kwargs(rank: int) -> dict:
+def replica_workload_kwargs(rank: int, config: int = WORKLOAD_CFG) -> dict:
     """Each replica packs its own batch: rank 0 the workload's own seed, rank r
     a seed of its own (same shapes and distributions, different values)."""
-    return {"seed": 2 + 1000 * rank} if rank else {}
+    return {"seed": DEFAULT_SEEDS[int(config)] + 1000 * rank} if rank else {}
 
 
 def max_over_ranks(dist, x: float, device) -> float:
@@ -96,19 +106,31 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
-    region (read-only queries)."""
+def n_rotating_sets(set_bytes: int, requested: int = 0) -> int:
+    """Buffer sets rotated between steps so that a set comes back only after
+    the others have moved more than the L2 holds (2 at least, 6 at most)."""
+    if requested > 0:
+        return int(requested)
+    return int(min(6, max(2, math.ceil(4 * L2_BYTES / max(set_bytes, 1)) + 1)))
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+
+class ClockSampler:
+    """nvidia-smi sampling (read-only queries) of SM clocks and throttle
+    reasons every 10 ms, with the sample's time stamp, so that the samples
+    taken inside a timed region can be told from the rest."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index: int, enabled: bool = True):
+    def __init__(self, gpu_index: int, enabled: bool = True, period_ms: int = 10):
         self.gpu = gpu_index
         self.enabled = enabled
+        self.period_ms = period_ms
         self.proc = None
         self.path = None
+        self.rows = []
 
     def start(self):
         if not self.enabled:
@@ -118,39 +140,56 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.period_ms), "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self) -> dict | None:
+    def stop(self):
+        """Ends the sampling and keeps the samples as (unix time, sm MHz,
+        max MHz, active reasons)."""
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        mhz, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
         try:
             for line in open(self.path):
                 f = [t.strip() for t in line.split(",")]
-                if len(f) < 9:
+                if len(f) < 10:
                     continue
                 try:
-                    mhz.append(float(f[1]))
-                    mx.append(float(f[2]))
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    mhz, mx = float(f[2]), float(f[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, f[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+                reasons = {n for n, v in zip(self.REASONS, f[6:10]) if v.lower() == "active"}
+                self.rows.append((ts, mhz, mx, reasons))
         finally:
             os.unlink(self.path)
-        if not mhz:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": float(np.median(mhz)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
-                "samples": len(mhz)}
+        self.proc = None
+
+    def summary(self, t0: float, t1: float, busy0: float | None = None) -> dict | None:
+        """Median SM clock and the reasons seen in [t0, t1] (unix times of the
+        timed region).  A region shorter than a few sampling periods may hold
+        no sample; then the samples of the busy period around it ([busy0, t1]:
+        the warm-up steps just before it and the region itself) are used, and
+        ``window`` says so."""
+        if not self.enabled:
+            return None
+        inside = [r for r in self.rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if len(inside) < 1 and busy0 is not None:
+            inside = [r for r in self.rows if busy0 <= r[0] <= t1 + self.period_ms * 1e-3]
+            window = "warm-up steps and timed region (the timed region alone is shorter than a sample period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        reasons = sorted(set().union(*[r[3] for r in inside]))
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": float(max(r[2] for r in inside)),
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "period_ms": self.period_ms}
 
 
 def source_sha(paths) -> str:
@@ -248,58 +287,48 @@ def capture_rotation(torch, sets, rotations: int = 1):
     return g
 
 
-def gpu_arm(args, rank, world, local):
-    import torch
-
-    import nvfp4_quantization_gb300 as nq
-    import workloads
-
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    def barrier():
-        if dist is not None:
-            dist.barrier(device_ids=[local])
-
-    w = workloads.make(args.config, **replica_workload_kwargs(rank))
+def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gpu_index=0):
+    """K steps of route plan + pack + direct receive on workload ``w``, timed
+    on the device.  ``n_sets`` buffer sets are rotated between steps (cold L2
+    per step); whole rotations run as CUDA graphs of up to 50 rotations (then
+    single steps for a remainder), so the device runs the steps back to back
+    with a launch gap only between graphs.  After the timed region one
+    rotation in ten is replayed call by call with CUDA events between the
+    calls, which gives the per-call durations of the roofline (those steps
+    stop the calls' overlap and are not part of the step time)."""
     T, H, k, E = w.T, w.H, w.k, w.E
     tok_host = torch.from_numpy(w.tokens.view(np.int16)).view(torch.bfloat16)
     topk_host = torch.from_numpy(np.ascontiguousarray(w.topk))
-    sets = [BufferSet(torch, nq, w, tok_host, topk_host) for _ in range(args.sets)]
+    S = nq.row_bytes(H)
+    R_cap = nq.rows_capacity(T, k, E, w.A)
+    set_bytes = 2 * T * H + 4 * T * k + R_cap * S * 2 + R_cap * (9 * H // 8 + 4)
+    nset = n_rotating_sets(set_bytes, n_sets)
+    sets = [BufferSet(torch, nq, w, tok_host, topk_host) for _ in range(nset)]
     torch.cuda.synchronize()
     st = int(sets[0].plan.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st:#x} after the first pass")
     R = int(sets[0].plan.offsets[-1].item())
-    S = nq.row_bytes(H)
     for b in sets:
         b.capture(torch)
-
-    # ---- timed region: K steps, rotating buffer sets (cold L2 per step).
-    # Steps go in blocks of one step per set; whole blocks run as graphs of up
-    # to GRAPH_ROTATIONS blocks each (then single steps for a remainder), so
-    # the device runs them back to back with a launch gap only between graphs.
     GRAPH_ROTATIONS = 50
-    gR = capture_rotation(torch, sets)
-    K, W = args.steps, args.warmup
-    nset = len(sets)
     SAMPLE_EVERY = 10
+    gR = capture_rotation(torch, sets)
     nblocks, rem = divmod(K, nset)
     n_big, n_small = divmod(nblocks, GRAPH_ROTATIONS)
     gBig = capture_rotation(torch, sets, GRAPH_ROTATIONS) if n_big else None
     gSmall = capture_rotation(torch, sets, n_small) if n_small else None
-    for i in range(max(1, W // nset)):
+    clocks = ClockSampler(gpu_index, enabled=clocks_enabled)
+    clocks.start()
+    time.sleep(0.1)
+    busy0 = time.time()
+    for i in range(max(1, math.ceil(W / nset))):   # at least W warm-up steps
         gR.replay()
     torch.cuda.synchronize()
-    barrier()
+    if barrier is not None:
+        barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local, enabled=not args.no_clocks)
-    clocks.start()
-    time.sleep(0.2)
-    wall0 = time.perf_counter()
+    wall0 = time.time()
     t0.record()
     for _ in range(n_big):
         gBig.replay()
@@ -309,15 +338,11 @@ def gpu_arm(args, rank, world, local):
         sets[j].gS.replay()
     t1.record()
     torch.cuda.synchronize()
-    wall1 = time.perf_counter()
-    clk = clocks.stop()
-    barrier()
-    ms_total = max_over_ranks(dist, t0.elapsed_time(t1), "cuda")
-    ms_step = ms_total / K
-    # ---- per-call durations for the roofline, after the timed region: one
-    # block in SAMPLE_EVERY again, each step replayed call by call with CUDA
-    # events between the calls (which stops the calls' overlap, so these steps
-    # are kept out of the step time)
+    wall1 = time.time()
+    time.sleep(0.03)
+    clocks.stop()
+    clk = clocks.summary(wall0, wall1, busy0)
+    ms_total = t0.elapsed_time(t1)
     n_sampled = max(1, (nblocks + SAMPLE_EVERY - 1) // SAMPLE_EVERY)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(nset)] for _ in range(n_sampled)]
@@ -336,16 +361,151 @@ def gpu_arm(args, rank, world, local):
     st = int(sets[0].plan.status.item())
     route_b, pack_b, dr_b = algorithmic_bytes(T, H, k, E, R, S)
     set_mb = (route_b + pack_b + dr_b) / 1e6
-    res = dict(set_mb=set_mb, T=T, H=H, k=k, E=E, R=R, S=S, ms_step=ms_step, ms_a=ms_a, ms_b=ms_b, wall_s=wall1 - wall0,
-               clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), world=world, w=w,
-               n_sampled_steps=len(flat))
+    return dict(sets=sets, tok_host=tok_host, topk_host=topk_host, nset=nset, set_mb=set_mb, T=T, H=H, k=k, E=E,
+                R=R, S=S, ms_total=ms_total, ms_step=ms_total / K, ms_a=ms_a, ms_b=ms_b, wall_s=wall1 - wall0,
+                clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), w=w, n_sampled_steps=len(flat), K=K, W=W)
 
+
+def step_report(r, peak, peak_kind, world=1, config=None, n_sets_note=True) -> dict:
+    """The JSON fields of one timed workload: throughput, path and per-call
+    rates, and the roofline block of the dominant kernel (the direct receive)."""
+    route_b, pack_b, dr_b = r["bytes"]
+    w = r["w"]
+    tokens_s = world * r["T"] / (r["ms_step"] * 1e-3)
+    dr_gbs = dr_b / (r["ms_b"] * 1e-3) / 1e9
+    pack_gbs = (route_b + pack_b) / (r["ms_a"] * 1e-3) / 1e9
+    path_gbs = (route_b + pack_b + dr_b) / (r["ms_step"] * 1e-3) / 1e9
+    cfg = {"workload": w.description, "T": r["T"], "H": r["H"], "E": r["E"], "k": r["k"], "A": w.A, "R": r["R"],
+           "rounding": "sr" if w.rounding else "rne",
+           "l2": f"{r['nset']} rotating buffer sets ({r['set_mb']:.0f} MB touched per step; a set is reused "
+                 f"after the others moved {(r['nset'] - 1) * r['set_mb']:.0f} MB through the 129 MB L2), "
+                 "back-to-back CUDA-graph steps",
+           "parallelism": f"replicas x{world}"}
+    return {
+        "value": tokens_s, "unit": UNIT, "ms_per_step": r["ms_step"], "steps": r["K"], "warmup": r["W"],
+        "config": cfg,
+        "path": {"gbs": path_gbs, "frac_of_peak": path_gbs / peak, "bytes_per_step": route_b + pack_b + dr_b,
+                 "route_pack_ms": r["ms_a"], "route_pack_gbs": pack_gbs, "route_pack_frac": pack_gbs / peak,
+                 "direct_receive_ms": r["ms_b"], "direct_receive_gbs": dr_gbs},
+        "roofline": {"kernel": "direct_receive_kernel (ep_nvfp4_direct_receive)", "bound": "hbm",
+                     "achieved": dr_gbs, "peak": peak, "unit": "GB/s", "frac": dr_gbs / peak,
+                     "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": dr_b,
+                     "traffic": profiled_traffic("direct_receive", DR_SOURCES, config)},
+        "clocks": r["clocks"],
+        "device_status": r["status"],
+        "sampled_steps_for_kernel_times": r["n_sampled_steps"],
+    }
+
+
+def gpu_arm(args, rank, world, local):
+    import torch
+
+    import nvfp4_quantization_gb300 as nq
+    import workloads
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier(device_ids=[local])
+
+    w = workloads.make(args.config, **replica_workload_kwargs(rank, args.config))
+    r = time_steps(torch, nq, w, args.steps, args.warmup, args.sets, barrier, not args.no_clocks, local)
+    r["ms_total"] = max_over_ranks(dist, r["ms_total"], "cuda")
+    r["ms_step"] = r["ms_total"] / args.steps
+    r["world"] = world
+    sets = r.pop("sets")
     # ---- end to end through the public API with host buffers
-    res["e2e"] = e2e_measure(torch, nq, w, sets[:2], tok_host, topk_host, R, args.e2e_steps)
-    res["e2e"]["ms"] = max_over_ranks(dist, res["e2e"]["ms"], "cuda")
-    # ---- the two calls outside the step: unpack and MXFP8 pack, same batch
-    res["aux"] = aux_measure(torch, nq, w, sets[0], R)
-    return res
+    e2e_steps = args.e2e_steps or int(min(200, max(20, 1000.0 / max(r["ms_step"] * 8, 1e-3))))
+    r["e2e"] = e2e_measure(torch, nq, w, sets[:2], r["tok_host"], r["topk_host"], r["R"], e2e_steps)
+    r["e2e"]["ms"] = max_over_ranks(dist, r["e2e"]["ms"], "cuda")
+    # ---- the calls outside the step: unpack, MXFP8 pack, the BF16 columnwise
+    # operands and the receive's variants, same batch
+    r["aux"] = aux_measure(torch, nq, w, sets[0], r["R"])
+    del sets
+    torch.cuda.empty_cache()
+    # ---- the other workloads (rank 0 of the replicas is enough: they are reports, not the headline)
+    r["extra"] = {}
+    r["config5"] = None
+    if not args.no_extra_configs and args.config == WORKLOAD_CFG:
+        peak, peak_kind = load_peaks()
+        for c, K in ((2, 3000), (3, 2000)):
+            wc = workloads.make(c, **replica_workload_kwargs(rank, c))
+            rc = time_steps(torch, nq, wc, K, max(args.warmup, 20), 0, None, not args.no_clocks, local)
+            del rc["sets"]
+            torch.cuda.empty_cache()
+            r["extra"][str(c)] = step_report(rc, peak, peak_kind, 1, c)
+        r["config5"] = config5_measure(torch, nq, workloads, rank, local, not args.no_clocks, peak, peak_kind)
+        torch.cuda.empty_cache()
+    return r
+
+
+def config5_measure(torch, nq, workloads, rank, local, clocks_enabled, peak, peak_kind) -> dict:
+    """The MXFP8 vs NVFP4 dispatch comparison on the StudentT(4) batch
+    (16384 x 7168, 64 experts top-6): the NVFP4 step timed like the headline
+    (RNE), both packs timed as single calls after an L2 flush, and the
+    relative RMS decode error of each format, sqrt(sum (decoded - x)^2 /
+    sum x^2) over every element of every token, from the GPU outputs (each
+    token's first destination row; its k rows are identical)."""
+    w = workloads.make(5, **replica_workload_kwargs(rank, 5))
+    rc = time_steps(torch, nq, w, 200, 20, 0, None, clocks_enabled, local)
+    out = step_report(rc, peak, peak_kind, 1, 5)
+    b = rc["sets"][0]
+    T, H, k, R_cap = w.T, w.H, w.k, b.plan.R_cap
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    mx = torch.empty(R_cap * H + R_cap * (H // 32), dtype=torch.uint8, device="cuda")
+
+    def timed(fn, reps=10):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    ms_mx = timed(lambda: nq.ep_mxfp8_pack(b.tok, b.plan, buf=mx))
+    ms_nv = timed(lambda: nq.ep_nvfp4_pack(b.tok, b.plan, rows=b.rows, rounding=w.rounding, seed=w.seed))
+    bytes_mx = 2 * T * H + 4 * T * k + rc["R"] * (H + H // 32)
+    bytes_nv = 2 * T * H + 4 * T * k + rc["R"] * rc["S"]
+    # decode errors, token by token against the BF16 input
+    first = b.plan.dest.view(T, k)[:, 0].long()
+    un = nq.ep_nvfp4_unpack(b.rows, H, b.plan.offsets, w.E, status=b.plan.status)
+    data = mx[: R_cap * H].view(R_cap, H)
+    scl = mx[R_cap * H:].view(R_cap, H // 32)
+    num_nv = num_mx = den = 0.0
+    for t0 in range(0, T, 1024):
+        rows_t = first[t0:t0 + 1024]
+        x = b.tok[t0:t0 + 1024].double()
+        d_nv = un[rows_t].double()
+        e = scl[rows_t].to(torch.int32) - 127
+        d_mx = data[rows_t].view(torch.float8_e4m3fn).double() * torch.pow(2.0, e.double()).repeat_interleave(32, 1)
+        num_nv += float(((d_nv - x) ** 2).sum())
+        num_mx += float(((d_mx - x) ** 2).sum())
+        den += float((x ** 2).sum())
+    torch.cuda.synchronize()
+    st = int(b.plan.status.item())
+    del rc["sets"], b, flush, mx, un
+    out["mxfp8_pack"] = {"ms": ms_mx, "gbs": bytes_mx / (ms_mx * 1e-3) / 1e9,
+                         "frac": bytes_mx / (ms_mx * 1e-3) / 1e9 / peak, "bytes": bytes_mx,
+                         "note": "one call (fused gather, E8M0 per 32, E4M3), L2 flushed before each launch"}
+    out["nvfp4_pack"] = {"ms": ms_nv, "gbs": bytes_nv / (ms_nv * 1e-3) / 1e9,
+                         "frac": bytes_nv / (ms_nv * 1e-3) / 1e9 / peak, "bytes": bytes_nv,
+                         "note": "one call on the same tokens and plan, L2 flushed before each launch"}
+    out["rms_rel_err"] = {"mxfp8": math.sqrt(num_mx / den), "nvfp4": math.sqrt(num_nv / den),
+                          "definition": "sqrt(sum (decoded - x)^2 / sum x^2) over all T x H elements; NVFP4 "
+                                        "decoded by ep_nvfp4_unpack, MXFP8 as E4M3 element x 2^(E8M0 - 127)"}
+    out["device_status"] = max(out["device_status"], st)
+    return out
 
 
 def aux_measure(torch, nq, w, b, R, reps=20):
@@ -458,8 +618,10 @@ def e2e_measure(torch, nq, w, bufs, tok_host, topk_host, R, steps):
     e1.record(main)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    ok = all(torch.equal(dsts[3][: 1 << 16].cuda(), srcs[3][: 1 << 16]) for _, _, srcs, dsts in lanes)
-    return dict(ms=ms, h2d=h2d, d2h=d2h, ok=bool(ok), link=host_link_gbs(torch))
+    # every output copied back by each lane's last step equals the device
+    # tensor it came from, whole (nothing writes them after that step)
+    ok = all(torch.equal(d.to(x.device), x) for _, _, srcs, dsts in lanes for x, d in zip(srcs, dsts))
+    return dict(ms=ms, h2d=h2d, d2h=d2h, ok=bool(ok), steps=steps, link=host_link_gbs(torch))
 
 
 def host_link_gbs(torch, nbytes: int = 256 << 20, reps: int = 5) -> dict:
@@ -511,59 +673,176 @@ def oracle_pass(o, w, tokens, topk):
     o.nvfp4_direct_receive(rows, w.H, off, w.E, rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask)
 
 
-def cpu_baseline(w, budget_s: float = 15.0) -> dict:
-    """The oracle, as it stands (single-threaded C), on the first n tokens of
-    the batch (and their routing), n sized from a 64-token probe so that the
-    timed pass takes about ``budget_s`` (the whole batch if that is shorter)."""
+def oracle_expert_pass(o, w, experts) -> int:
+    """The batch's route plan + pack + direct receive on the oracle,
+    restricted to the experts in ``experts``: every routing slot to another
+    expert is dropped, so each kept expert has exactly its rows (and padding)
+    of the whole batch, the pack writes only those rows and the receive
+    builds only those experts' operands.  Returns the number of routed slots
+    kept; slots / k is the batch's work in tokens that the pass did."""
+    topk = np.array(w.topk, copy=True)
+    topk[~np.isin(topk, np.asarray(list(experts), dtype=np.int32))] = -1
+    off, cnt, dest, _ = o.route_plan(topk, w.E, w.A)
+    R_cap = int(off[-1])
+    rows = o.nvfp4_pack(w.tokens, dest, w.k, off, cnt, w.E, max(R_cap, 1), rounding=w.rounding, seed=w.seed)
+    o.nvfp4_direct_receive(rows, w.H, off, w.E, rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask,
+                           experts=list(experts))
+    return int(np.count_nonzero(topk >= 0))
+
+
+def expert_loads(w) -> list[tuple[int, int]]:
+    """(expert, routed slots) of every expert with at least one slot."""
+    ids, counts = np.unique(w.topk[w.topk >= 0], return_counts=True)
+    return [(int(e), int(c)) for e, c in zip(ids, counts)]
+
+
+def expert_groups(loads, n_groups: int) -> list[list[int]]:
+    """Experts split into n_groups of about equal slots (largest first, each
+    to the least loaded group)."""
+    groups = [[] for _ in range(n_groups)]
+    tot = [0] * n_groups
+    for e, c in sorted(loads, key=lambda x: -x[1]):
+        g = int(np.argmin(tot))
+        groups[g].append(e)
+        tot[g] += c
+    return [sorted(g) for g in groups if g]
+
+
+def host_cpu() -> dict:
+    """The host's logical CPU count and model name (lscpu, else /proc/cpuinfo)."""
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not name:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    name = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    return {"nproc": n, "model": name or "unknown"}
+
+
+_SLICE_W = None
+
+
+def _oracle_group_init(cfg: int, kw: dict):
+    """Pool initializer of the all-core baseline: the workload and the oracle,
+    made once per process before any timed task."""
+    global _SLICE_W
+    import oracle as o
+    import workloads
+    _SLICE_W = workloads.make(cfg, **kw)
+    o.lib()
+
+
+def _oracle_group_worker(experts):
+    """One task of the all-core baseline: the oracle's pass over one group
+    of experts; returns (start, end) wall-clock seconds and the slots done."""
+    import oracle as o
+    t0 = time.time()
+    n = oracle_expert_pass(o, _SLICE_W, experts) if experts else 0
+    return t0, time.time(), n
+
+
+def cpu_baseline(w, cfg: int, budget_s: float = 10.0, all_cores: bool = True, kw: dict | None = None) -> dict:
+    """The oracle, as it stands (single-threaded C), timed on a bounded sample
+    of the batch: the route plan, pack and direct receive restricted to the
+    first m experts (each with exactly its rows and padding of the whole
+    batch), m sized from a one-expert probe for about ``budget_s``; value =
+    (routed slots kept / k) / seconds, i.e. tokens of the batch per second.
+    Then the whole batch on all host cores: its experts split into one group
+    per core (about equal slots), one process per group, started together;
+    value = tokens of the batch / (last end - first start)."""
     import oracle as o
     o.build()
+    loads = expert_loads(w)
     t0 = time.perf_counter()
-    oracle_pass(o, w, np.ascontiguousarray(w.tokens[:64]), np.ascontiguousarray(w.topk[:64]))
-    per_tok = (time.perf_counter() - t0) / 64
-    n = int(max(64, min(w.T, budget_s / max(per_tok, 1e-9))))
-    tok, topk = np.ascontiguousarray(w.tokens[:n]), np.ascontiguousarray(w.topk[:n])
+    s1 = oracle_expert_pass(o, w, [loads[0][0]])
+    per_slot = (time.perf_counter() - t0) / max(s1, 1)
+    m, acc = 0, 0
+    while m < len(loads) and (m == 0 or (acc + loads[m][1]) * per_slot <= budget_s):
+        acc += loads[m][1]
+        m += 1
+    experts = [e for e, _ in loads[:m]]
     t0 = time.perf_counter()
-    oracle_pass(o, w, tok, topk)
+    slots = oracle_expert_pass(o, w, experts)
     dt = time.perf_counter() - t0
-    what = "the full batch" if n == w.T else f"the first {n} of {w.T} tokens"
-    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"one pass over {what} (route plan + pack + direct receive), single-threaded C oracle, "
-                      f"{dt:.2f} s"}
+    hc = host_cpu()
+    res = {"value": slots / w.k / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "host_cpu": hc["model"],
+           "nproc": hc["nproc"],
+           "sample": f"route plan + pack + direct receive of {m} of the batch's {len(loads)} routed experts "
+                     f"({slots} of {int(np.count_nonzero(w.topk >= 0))} slots, each expert with its rows and "
+                     f"padding of the whole batch), single-threaded C oracle, {dt:.2f} s; tokens = slots / k"}
+    if all_cores and hc["nproc"] > 1:
+        import multiprocessing as mp
+        C = hc["nproc"]
+        groups = expert_groups(loads, C)
+        with mp.get_context("spawn").Pool(len(groups), initializer=_oracle_group_init,
+                                          initargs=(cfg, kw or {})) as pool:
+            # a short task per process first, so that every process has made
+            # its workload before the timed tasks start
+            pool.map(_oracle_group_worker, [[]] * (2 * len(groups)), chunksize=1)
+            spans = pool.map(_oracle_group_worker, groups, chunksize=1)
+        wall = max(e for _, e, _ in spans) - min(s for s, _, _ in spans)
+        slots_all = sum(n for _, _, n in spans)
+        res["all_cores"] = {"value": slots_all / w.k / wall, "unit": UNIT, "cores": len(groups), "wall_s": wall,
+                            "sample": f"the whole batch: its experts in {len(groups)} groups of about equal slots, "
+                                      "one process per group (the unchanged single-threaded oracle) started "
+                                      "together; tokens / (last end - first start)"}
+        res["cores_all"] = len(groups)
+    return res
 
 
 def reference_arm(args, rank, world):
-    """--impl reference: the oracle on the host cores, each step a slice of
-    the same workload sized so that warm-up + K steps take about two minutes."""
+    """--impl reference: the oracle on the host cores, single-threaded; each
+    step is the route plan + pack + direct receive of a group of the batch's
+    experts (each with its rows and padding of the whole batch; groups taken
+    in turn), the group sized so that warm-up + K steps take about two
+    minutes; value = (routed slots / k) / seconds."""
     if rank != 0:
         return None
     import oracle as o
     import workloads
     o.build()
     w = workloads.make(args.config)
+    loads = expert_loads(w)
     t0 = time.perf_counter()
-    oracle_pass(o, w, w.tokens[:512], w.topk[:512])
-    per_tok = (time.perf_counter() - t0) / 512
+    s1 = oracle_expert_pass(o, w, [loads[0][0]])
+    per_slot = (time.perf_counter() - t0) / max(s1, 1)
     K, W = args.steps, args.warmup
-    n = int(max(1, min(w.T, 120.0 / max(K + W, 1) / per_tok)))
-
-    def run(i):
-        a = (i * n) % w.T
-        idx = np.arange(a, a + n) % w.T
-        oracle_pass(o, w, np.ascontiguousarray(w.tokens[idx]), np.ascontiguousarray(w.topk[idx]))
-
+    budget = 120.0 / max(K + W, 1)
+    m = int(max(1, min(len(loads), budget / max(per_slot * np.mean([c for _, c in loads]), 1e-9))))
+    groups = [[loads[(i * m + j) % len(loads)][0] for j in range(m)] for i in range(K + W)]
     for i in range(W):
-        run(i)
+        oracle_expert_pass(o, w, groups[i])
+    slots = 0
     t0 = time.perf_counter()
     for i in range(K):
-        run(W + i)
+        slots += oracle_expert_pass(o, w, groups[W + i])
     dt = time.perf_counter() - t0
-    value = n * K / dt
+    value = slots / w.k / dt
+    hc = host_cpu()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": dt * 1e3 / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.description, "tokens_per_step": n},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{n} consecutive tokens of the batch (and their routing) per step"},
+            "config": {"workload": w.description, "experts_per_step": m, "tokens_per_step": slots / w.k / max(K, 1)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "host_cpu": hc["model"],
+                             "nproc": hc["nproc"],
+                             "sample": f"per step the route plan + pack + direct receive of {m} of the batch's "
+                                       f"{len(loads)} routed experts (each with its rows and padding of the whole "
+                                       "batch; groups in turn); tokens = routed slots / k"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     return line
 
@@ -580,32 +859,18 @@ def main():
     if rank != 0:
         return
     peak, peak_kind = load_peaks()
-    route_b, pack_b, dr_b = r["bytes"]
     w = r["w"]
-    tokens_s = world * r["T"] / (r["ms_step"] * 1e-3)
-    dr_gbs = dr_b / (r["ms_b"] * 1e-3) / 1e9
-    pack_gbs = (route_b + pack_b) / (r["ms_a"] * 1e-3) / 1e9
-    path_gbs = (route_b + pack_b + dr_b) / (r["ms_step"] * 1e-3) / 1e9
+    rep = step_report(r, peak, peak_kind, world, args.config)
     e2e = r["e2e"]
     line = {
-        "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": rep["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.description, "T": r["T"], "H": r["H"], "E": r["E"], "k": r["k"], "A": w.A,
-                   "R": r["R"], "rounding": "sr" if w.rounding else "rne",
-                   "l2": f"{args.sets} rotating buffer sets ({r['set_mb']:.0f} MB touched per step; a set is reused "
-                         f"after the others moved {(args.sets - 1) * r['set_mb']:.0f} MB through the 129 MB L2), "
-                         "back-to-back CUDA-graph steps",
-                   "parallelism": f"replicas x{world}"},
-        "path": {"gbs": path_gbs, "frac_of_peak": path_gbs / peak, "bytes_per_step": route_b + pack_b + dr_b,
-                 "route_pack_ms": r["ms_a"], "route_pack_gbs": pack_gbs, "direct_receive_ms": r["ms_b"],
-                 "direct_receive_gbs": dr_gbs},
-        "roofline": {"kernel": "direct_receive_kernel (ep_nvfp4_direct_receive)", "bound": "hbm",
-                     "achieved": dr_gbs, "peak": peak, "unit": "GB/s", "frac": dr_gbs / peak,
-                     "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": dr_b,
-                     "traffic": profiled_traffic("direct_receive", DR_SOURCES, args.config)},
+        "config": rep["config"],
+        "path": rep["path"],
+        "roofline": rep["roofline"],
         "e2e": {"value": world * r["T"] / (e2e["ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
-                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"],
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"], "steps": e2e["steps"],
                 "api": "eager ep_nvfp4_dispatch / ep_nvfp4_direct_receive on two streams, "
                        "alternate steps (double buffering)", "checked": e2e["ok"],
                 "host_link_gbs": e2e["link"],
@@ -624,8 +889,12 @@ def main():
         "device_status": r["status"],
         "timed_wall_s": r["wall_s"],
     }
+    if r["extra"]:
+        line["configs"] = r["extra"]
+    if r["config5"] is not None:
+        line["config5"] = r["config5"]
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, args.config)
     print(json.dumps(line), flush=True)
 
 

@@ -34,7 +34,7 @@ def rank_main(rank, world, port, out):
         # the slowest rank's time, on every rank
         t = bench.max_over_ranks(dist, 10.0 + 5.0 * rank, "cpu")
         # each rank's own batch of the same shape
-        w = workloads.make(1, T=64, H=256, **bench.replica_workload_kwargs(rank))
+        w = workloads.make(1, T=64, H=256, **bench.replica_workload_kwargs(rank, 1))
         digest = float(np.asarray(w.tokens, np.float64).sum())
         # the reference arm: rank 0 only
         args = type("A", (), {"steps": 1, "warmup": 0, "config": 1})()
@@ -60,4 +60,6 @@ def test_one_process_needs_no_collective():
     import bench
     assert bench.max_over_ranks(None, 3.5, "cpu") == 3.5
     assert bench.replica_workload_kwargs(0) == {}
-    assert bench.replica_workload_kwargs(3) == {"seed": 3002}
+    assert bench.replica_workload_kwargs(3, 2) == {"seed": 3002}
+    # the default workload is the largest configuration (seed 4)
+    assert bench.replica_workload_kwargs(3) == {"seed": 3004}
