@@ -60,9 +60,6 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers;         // no producer warp: the last warp to free a stage refills it
 constexpr uint32_t kStageTx = kTileRows * (kCodeBytes + kScaleBytes + 16);
-constexpr int kWarpRows = kTileRows / 2;     // rows of a tile one consumer warp handles
-constexpr int kWTabStride = kWarpRows + 2;   // float2 entries; pad: a warp's 4 column blocks hit distinct banks
-constexpr int kT16Stride = kWarpRows + 4;    // f16 entries of the f16 table (same storage); distinct banks too
 constexpr int kMaxExperts = 1024;
 
 struct StageMeta {
@@ -76,33 +73,41 @@ struct __align__(128) DrSmem {
     uint8_t codes[NS][kTileRows][kCodeBytes];
     uint8_t scales[NS][kTileRows][kScaleBytes];
     uint32_t trailer[NS][kTileRows][4];
-    float2 wtab[kConsumerWarps][4][kWTabStride]; // per warp: [column block][row] decode scale, twice
-    float wrtab[kConsumerWarps][128];           // per warp: [E4M3 code s] -> fl32(S_enc / s) of its expert
+    union {   // rows padded to 80 bytes: the 16 column blocks' rows start on different banks
+        uint2 t16[kConsumerWarps][16][10];       // per warp: [column block][row pair] (w2, w2 with -w_b)
+        float t32[kConsumerWarps][16][20];       // per warp: [column block][row] FP32 decode scale
+    } tab;
+    uint8_t outc[2][kConsumerWarps][2048];       // [tile parity][warp = row block]: 256 columns x 8 code bytes
+    uint8_t outs[2][kConsumerWarps][256];        // [tile parity][warp]: a scale byte per column
     float rcp[128];                             // [E4M3 code s] -> RN(1 / s), 0 for s = 0
-    uint32_t csc[NS][kConsumerWarps / 2][32][2]; // [stage][column quarter][lane]: scales of rows 64..127
     StageMeta meta[NS];
-    float se_cache[kMaxExperts];                // S_enc of every expert
-    int offs[kMaxExperts + 1];                  // expert_offsets, copied once
     uint64_t full[NS];
+    uint64_t stg_full[2];                       // outc / outs [parity] written by all 8 warps
     uint32_t rel[NS];                      // warps done with the stage's current tile
-    uint64_t csc_full[NS][kConsumerWarps / 2];   // csc[stage][quarter] written
     int abort_flag;
     int consumed;                               // fewest tiles any warp finished
     int issued;                                 // tiles whose loads were issued
+    // followed, in the launch's dynamic shared memory, by expert_offsets
+    // (E + 1 ints, copied once) and the S_enc of every expert (E floats)
 };
 
-// two CTAs per SM: each gets at most (228 KB - 2 x 1 KB reserved) / 2
-// RNE: two stages and three CTAs per SM (80 registers suffice); SR: three
-// stages and two CTAs per SM (the Philox state needs 128 registers)
+template <class Sm>
+__device__ __forceinline__ int *smem_offs(Sm &sm) { return reinterpret_cast<int *>(&sm + 1); }
+template <class Sm>
+__device__ __forceinline__ float *smem_se(Sm &sm, int E) { return reinterpret_cast<float *>(smem_offs(sm) + E + 1); }
+
+// Three ring stages and two CTAs per SM in both modes: a thread holds its 16
+// code words, its 8 decode-scale pairs and the 16 butterfly pairs, which
+// needs more than the 80 registers three CTAs per SM would leave.
 template <bool kSR>
 struct DrCfg {
-    static constexpr int kStages = kSR ? 3 : 2;
-    static constexpr int kCtasPerSm = kSR ? 2 : 3;
+    static constexpr int kStages = 3;
+    static constexpr int kCtasPerSm = 2;
     using Smem = DrSmem<kStages>;
 };
 // each CTA gets at most (228 KB - 1 KB reserved per CTA) / CTAs per SM
-static_assert(sizeof(DrCfg<true>::Smem) + 1024 <= 113 * 1024, "SR direct receive must fit two CTAs per SM");
-static_assert(sizeof(DrCfg<false>::Smem) + 1024 <= 75 * 1024, "RNE direct receive must fit three CTAs per SM");
+// (with the per-expert arrays of up to 256 experts)
+static_assert(sizeof(DrCfg<true>::Smem) + 1024 + 8 * 256 + 4 <= 113 * 1024, "direct receive must fit two CTAs per SM");
 
 struct DrArgs {
     const uint8_t *rows;
@@ -180,10 +185,11 @@ __device__ __forceinline__ bool tile_of(const DrArgs &p, int n_units, int it, in
 template <class Sm>
 __device__ __forceinline__ void stage_meta(Sm &sm, const DrArgs &p, int s, int rt)
 {
-    const int e = expert_of_row(sm.offs, p.E, rt * kTileRows);
-    const int off = sm.offs[e];
-    const float se = sm.se_cache[e];
-    sm.meta[s] = StageMeta{e, off, sm.offs[e + 1] - off, se, __fdiv_rn(se, 6.0f)};
+    const int *offs = smem_offs(sm);
+    const int e = expert_of_row(offs, p.E, rt * kTileRows);
+    const int off = offs[e];
+    const float se = smem_se(sm, p.E)[e];
+    sm.meta[s] = StageMeta{e, off, offs[e + 1] - off, se, __fdiv_rn(se, 6.0f)};
 }
 
 // Per-expert metadata (one CTA per expert, grid-stride): the rowwise amax is
@@ -252,45 +258,68 @@ __device__ __forceinline__ void st32g(void *p, uint4 a, uint4 b)
                  : "memory");
 }
 
-// One 16-row block of the thread's two columns: decode, RHT, block scales,
-// E2M1 codes.  Returns the 8 code bytes of each column (cw0, cw1) and the two
-// E4M3 scale codes (s2: column 0 in the low byte).
-template <bool kSR, bool kFastR, bool kF16, class Sm>
-__device__ __forceinline__ void rht_block(const Sm &sm, int s, const void *tab, const float *rtab, int c,
-                                          int r0, float ce, float se, const DrArgs &p, const StageMeta &m, int h0,
-                                          int rl, uint2 &cw0, uint2 &cw1, uint32_t &s2)
+// Byte P of a word of code bytes -> f16x2 of its two E2M1 codes (exact; the
+// low nibble to the low half).
+template <int P>
+__device__ __forceinline__ uint32_t e2m1_byte_f16x2(uint32_t w)
+{
+    uint32_t r;
+    if (P == 0)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+            : "=r"(r) : "r"(w));
+    else if (P == 1)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}"
+            : "=r"(r) : "r"(w));
+    else if (P == 2)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}"
+            : "=r"(r) : "r"(w));
+    else
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}"
+            : "=r"(r) : "r"(w));
+    return r;
+}
+
+// Byte offset, in a warp's code staging area (256 columns x 8 bytes: its
+// 16-row block of every column of the strip), of columns 8l + 2p and
+// 8l + 2p + 1: lane l's 64 bytes with their 16-byte chunks rotated by l mod 4,
+// so that the 32 lanes' 16-byte stores of one column pair fall on distinct
+// banks.
+__device__ __forceinline__ int stage_off(int l, int p) { return 64 * l + 16 * (p ^ (l & 3)); }
+
+// The thread's 16-row block of 8 columns, one column pair (code byte P of
+// the 16 code words) at a time: decode, the RHT, block scales, E2M1 codes
+// (RNE, or SR with the Philox words of the pair's two columns).  The pair's
+// 16 code bytes and 2 scale bytes go to the warp's staging areas.
+//   kF16: t16 holds the 8 row pairs' (w2, -w2 high) decode-scale words as
+//   f16 pairs, values scaled by 2^-K (se, ce scaled by 2^K); else t32 holds
+//   the 16 rows' FP32 decode scales and r = S_enc / s is an IEEE division.
+template <bool kSR, bool kF16, int P>
+__device__ __forceinline__ void rht_pair(const uint32_t (&cw)[16], const uint2 (&t16)[8], const float (&t32)[16],
+                                         const float *rcp, float se, float ce, const Philox4 &ra, const Philox4 &rb,
+                                         uint8_t *outc, uint8_t *outs, int lane)
 {
     float2 u[16];
     if (kF16) {
-        // tab: the column block's decode scales of rows r0 .. r0+15 as f16,
-        // rows (i, i+1) in one word, scaled by the warp tile's 2^-K; each
-        // decoded value q w is an exact f16 x f16 product, made and summed by
-        // one mixed-precision FMA (the same single rounding as below)
-        const uint32_t *tp = reinterpret_cast<const uint32_t *>(tab);
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-            const uint32_t w2 = tp[i >> 1];
-            const uint32_t qa = cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i][c]);
-            const uint32_t qb = cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i + 1][c]);
-            const uint32_t nqb = qb ^ 0x80008000u;
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w2 = t16[i].x, nw2 = t16[i].y;
+            const uint32_t qa = e2m1_byte_f16x2<P>(cw[2 * i]);
+            const uint32_t qb = e2m1_byte_f16x2<P>(cw[2 * i + 1]);
+            // d_a = q_a w_a exactly (f16 x f16 in FP32), then the len-1
+            // butterfly d_a +- q_b w_b with one rounding each
             const float dax = fma_f16h<0, 0>(qa, w2, -0.0f), day = fma_f16h<1, 0>(qa, w2, -0.0f);
-            u[i] = make_float2(fma_f16h<0, 1>(qb, w2, dax), fma_f16h<1, 1>(qb, w2, day));
-            u[i + 1] = make_float2(fma_f16h<0, 1>(nqb, w2, dax), fma_f16h<1, 1>(nqb, w2, day));
+            u[2 * i] = make_float2(fma_f16h<0, 1>(qb, w2, dax), fma_f16h<1, 1>(qb, w2, day));
+            u[2 * i + 1] = make_float2(fma_f16h<0, 1>(qb, nw2, dax), fma_f16h<1, 1>(qb, nw2, day));
         }
     } else {
-        // tab: this column block's decode scales of rows r0 .. r0+15, as (sc, sc)
-        const float4 *tp = reinterpret_cast<const float4 *>(tab);
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-            const float4 t4 = tp[i >> 1];
-            const float2 qa = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i][c]));
-            const float2 qb = f16x2_to_f32x2(cvt_f16x2_from_e2m1x2(sm.codes[s][r0 + i + 1][c]));
-            // len = 1 butterflies on the decoded values, which are exact products:
-            // one rounding each, fl(da + qb tb) and fl(da - qb tb), as a fused
-            // multiply-add with the exact product qb tb gives
-            const float2 da = mul2(qa, make_float2(t4.x, t4.y));
-            u[i] = __ffma2_rn(qb, make_float2(t4.z, t4.w), da);
-            u[i + 1] = __ffma2_rn(qb, make_float2(-t4.z, -t4.w), da);
+        for (int i = 0; i < 8; ++i) {
+            const float wa = t32[2 * i], wb = t32[2 * i + 1];
+            const float2 qa = f16x2_to_f32x2(e2m1_byte_f16x2<P>(cw[2 * i]));
+            const float2 qb = f16x2_to_f32x2(e2m1_byte_f16x2<P>(cw[2 * i + 1]));
+            const float2 da = mul2(qa, make_float2(wa, wa));
+            u[2 * i] = __ffma2_rn(qb, make_float2(wb, wb), da);
+            u[2 * i + 1] = __ffma2_rn(qb, make_float2(-wb, -wb), da);
         }
     }
     // remaining Walsh-Hadamard butterflies, len = 2, 4, 8
@@ -305,52 +334,109 @@ __device__ __forceinline__ void rht_block(const Sm &sm, int s, const void *tab, 
             u[a + len] = sub2(x, y);
         }
     }
-    // block maxima as a tree of 3-input maxima (depth 3, not a chain of 7)
+    // block maxima as a tree of 3-input maxima
     const float p0 = max3_abs(fabsf(u[0].x), u[1].x, u[2].x), q0 = max3_abs(fabsf(u[0].y), u[1].y, u[2].y);
     const float p1 = max3_abs(fabsf(u[3].x), u[4].x, u[5].x), q1 = max3_abs(fabsf(u[3].y), u[4].y, u[5].y);
     const float p2 = max3_abs(fabsf(u[6].x), u[7].x, u[8].x), q2 = max3_abs(fabsf(u[6].y), u[7].y, u[8].y);
     const float p3 = max3_abs(fabsf(u[9].x), u[10].x, u[11].x), q3 = max3_abs(fabsf(u[9].y), u[10].y, u[11].y);
     const float p4 = max3_abs(fabsf(u[12].x), u[13].x, u[14].x), q4 = max3_abs(fabsf(u[12].y), u[13].y, u[14].y);
-    const float b0 = fmaxf(fmaxf(p0, p1), max3_abs(fmaxf(p2, p3), p4, u[15].x));
-    const float b1 = fmaxf(fmaxf(q0, q1), max3_abs(fmaxf(q2, q3), q4, u[15].y));
-    s2 = cvt_e4m3x2(b0 * ce, b1 * ce);
+    const float b0 = max3_abs(max3_abs(p0, p1, p2), p3, max3_abs(p4, u[15].x, 0.0f));
+    const float b1 = max3_abs(max3_abs(q0, q1, q2), q3, max3_abs(q4, u[15].y, 0.0f));
+    const float2 bc = mul2(make_float2(b0, b1), make_float2(ce, ce));
+    const uint32_t s2 = cvt_e4m3x2(bc.x, bc.y);
     float2 r2;
-    if (kFastR) {
+    if (kF16) {
         // r = fl32(S_enc / s) by one Markstein step from y = RN(1/s): q = RN(S_enc y),
         // e = S_enc - s q (exact), r = RN(q + e y) is the correctly rounded
-        // quotient (S_enc within 2^(+-100): nothing overflows or underflows);
-        // s = 0 gives y = 0 and r = 0
-        const float2 y2 = make_float2(sm.rcp[s2 & 0xffu], sm.rcp[(s2 >> 8) & 0xffu]);
-        const float2 sv = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(s2 & 0xffffu));
+        // quotient (S_enc within 2^(+-100)); s = 0 gives y = 0 and r = 0
+        const float2 y2 = make_float2(rcp[s2 & 0xffu], rcp[(s2 >> 8) & 0xffu]);
+        const float2 sv = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(s2));
         const float2 se2 = make_float2(se, se);
         const float2 q = mul2(se2, y2);
         const float2 e = __ffma2_rn(make_float2(-sv.x, -sv.y), q, se2);
         r2 = __ffma2_rn(e, y2, q);
     } else {
-        r2 = make_float2(rtab[s2 & 0xffu], rtab[(s2 >> 8) & 0xffu]);
+        const float2 sv = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(s2));
+        r2 = make_float2(sv.x == 0.0f ? 0.0f : __fdiv_rn(se, sv.x), sv.y == 0.0f ? 0.0f : __fdiv_rn(se, sv.y));
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i)
         u[i] = mul2(u[i], r2);
+    uint4 cc;
     if (kSR) {
         // rows 4q .. 4q + 3 of the block take word q of its column's Philox output
-        const uint64_t pos = (uint64_t)m.off * (uint64_t)p.H + (uint64_t)h0 * (uint64_t)m.n + (uint64_t)(rl + r0);
-        const Philox4 ra = sr_bytes16(p.key, 1u, pos);
-        const Philox4 rb = sr_bytes16(p.key, 1u, pos + (uint64_t)m.n);
-        cw0 = make_uint2(cvt_e2m1x8_sr(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x, ra.x, ra.y),
-                         cvt_e2m1x8_sr(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x, ra.z,
-                                       ra.w));
-        cw1 = make_uint2(cvt_e2m1x8_sr(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y, rb.x, rb.y),
-                         cvt_e2m1x8_sr(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y, rb.z,
-                                       rb.w));
-        return;
+        cc = make_uint4(cvt_e2m1x8_sr(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x, ra.x, ra.y),
+                        cvt_e2m1x8_sr(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x, ra.z,
+                                      ra.w),
+                        cvt_e2m1x8_sr(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y, rb.x, rb.y),
+                        cvt_e2m1x8_sr(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y, rb.z,
+                                      rb.w));
+    } else {
+        cc = make_uint4(cvt_e2m1x8(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x),
+                        cvt_e2m1x8(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x),
+                        cvt_e2m1x8(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y),
+                        cvt_e2m1x8(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y));
     }
-    cw0 = make_uint2(cvt_e2m1x8(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x),
-                     cvt_e2m1x8(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x));
-    cw1 = make_uint2(cvt_e2m1x8(u[0].y, u[1].y, u[2].y, u[3].y, u[4].y, u[5].y, u[6].y, u[7].y),
-                     cvt_e2m1x8(u[8].y, u[9].y, u[10].y, u[11].y, u[12].y, u[13].y, u[14].y, u[15].y));
+    *reinterpret_cast<uint4 *>(outc + stage_off(lane, P)) = cc;
+    *reinterpret_cast<uint16_t *>(outs + 8 * lane + 2 * P) = (uint16_t)s2;
 }
 
+// The Philox outputs of columns h and h + 1 of one 16-row block: counters
+// n and n + nstep (n = (off_e H + h n_e + row) / 16, nstep = n_e / 16).
+__device__ __forceinline__ void pair_random(const PhiloxKey &K, uint64_t n, uint32_t nstep, Philox4 &ra, Philox4 &rb)
+{
+    const uint64_t n1 = n + nstep;
+    ra = philox4x32_10((uint32_t)n, (uint32_t)(n >> 32), 1u, 0u, K);
+    rb = philox4x32_10((uint32_t)n1, (uint32_t)(n1 >> 32), 1u, 0u, K);
+}
+
+// The thread's four column pairs (8 columns x 16 rows).  With stochastic
+// rounding the Philox outputs of the next pair are computed alongside the
+// current pair's arithmetic (independent work for the scheduler).
+template <bool kSR, bool kF16>
+__device__ __forceinline__ void rht_thread(const uint32_t (&cw)[16], const uint2 (&t16)[8], const float (&t32)[16],
+                                           const float *rcp, float se, float ce, const PhiloxKey &K, uint64_t nbase,
+                                           uint32_t nstep, uint8_t *outc, uint8_t *outs, int lane)
+{
+    Philox4 ra, rb, na, nb;
+    if (kSR)
+        pair_random(K, nbase, nstep, ra, rb);
+    if (kSR)
+        pair_random(K, nbase + 2 * (uint64_t)nstep, nstep, na, nb);
+    rht_pair<kSR, kF16, 0>(cw, t16, t32, rcp, se, ce, ra, rb, outc, outs, lane);
+    if (kSR) {
+        ra = na;
+        rb = nb;
+        pair_random(K, nbase + 4 * (uint64_t)nstep, nstep, na, nb);
+    }
+    rht_pair<kSR, kF16, 1>(cw, t16, t32, rcp, se, ce, ra, rb, outc, outs, lane);
+    if (kSR) {
+        ra = na;
+        rb = nb;
+        pair_random(K, nbase + 6 * (uint64_t)nstep, nstep, na, nb);
+    }
+    rht_pair<kSR, kF16, 2>(cw, t16, t32, rcp, se, ce, ra, rb, outc, outs, lane);
+    rht_pair<kSR, kF16, 3>(cw, t16, t32, rcp, se, ce, na, nb, outc, outs, lane);
+}
+
+// The FP32-table path (a row block whose token exponents spread too far for
+// the f16 decode scales): rare, kept out of line.
+template <bool kSR>
+__device__ __noinline__ void rht_thread_f32(const uint32_t (&cw)[16], const float (&t32)[16], const float *rcp,
+                                            float se, float ce, const PhiloxKey &K, uint64_t nbase, uint32_t nstep,
+                                            uint8_t *outc, uint8_t *outs, int lane)
+{
+    const uint2 t16[8] = {};
+    rht_thread<kSR, false>(cw, t16, t32, rcp, se, ce, K, nbase, nstep, outc, outs, lane);
+}
+
+// Warp w computes row block w (rows 16w .. 16w + 15) of the tile, lane l the
+// columns 8l .. 8l + 7 of the strip (the code bytes 4l .. 4l + 3 of each row:
+// a warp's loads cover whole 128-byte rows).  A column's 128 rows thus come
+// from all 8 warps: each warp stages its 8 code bytes and one scale byte per
+// column, the 8 warps meet at an mbarrier (double-buffered staging, so once
+// per tile), and thread c then stores column c's 64 code bytes (two full
+// sectors) and 8 scale bytes.
 template <bool kSR, bool kSwz, class Sm>
 __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, const CUtensorMap *tm_rws,
                                              const CUtensorMap *tmc, const CUtensorMap *tms,
@@ -358,13 +444,8 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
 {
     const int c = threadIdx.x;          // 0 .. kConsumers-1
     const int warp = c >> 5, lane = c & 31;
-    const int hh = warp >> 2;           // rows [64 hh, 64 hh + 64) of the tile
-    const int cq = warp & 3;            // column pairs [32 cq, 32 cq + 32) of the strip
-    const int pc = 32 * cq + lane;      // this thread's column pair
     const int H = p.H;
-    float2(*tab)[kWTabStride] = sm.wtab[warp];
     int done = 0;
-    int cur_e = -1;   // expert whose S_enc / s table this warp holds
     int rt, st;
     for (int it = 0; tile_of(p, n_units, it, rt, st); ++it) {
         const int s = it % Sm::kNS;
@@ -379,6 +460,9 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
         const StageMeta m = sm.meta[s];
         const int row0 = rt * kTileRows;
         const int rl = row0 - m.off;
+        const int par = it & 1;
+        uint8_t *outc = sm.outc[par][warp];
+        uint8_t *outs = sm.outs[par][warp];
 
         // rowwise operand: codes by TMA store, scales and token scale by threads
         if (p.do_rowwise && c < kTileRows) {
@@ -408,174 +492,103 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
             uint8_t *run = p.rw_scales + ((int64_t)rt * (H / 64) + 4 * st) * 512;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int w = c + kThreads * j, g = w >> 7, i = (w >> 2) & 31, q = w & 3;
-                if (g < ng)
+                const int w = c + kThreads * j, gg = w >> 7, i = (w >> 2) & 31, q = w & 3;
+                if (gg < ng)
                     *reinterpret_cast<uint32_t *>(run + 4 * w) =
-                        *reinterpret_cast<const uint32_t *>(&sm.scales[s][32 * q + i][4 * g]);
+                        *reinterpret_cast<const uint32_t *>(&sm.scales[s][32 * q + i][4 * gg]);
             }
         }
 
-        // this warp's decode scales: rows 64 hh + {lane, lane + 32}, column
-        // blocks 4 cq .. 4 cq + 3, with the RHT sign and the 1/4 folded in.
-        // When the token exponents k of the warp's rows with a nonzero scale
-        // lie within 13 of their maximum K, every s_b 2^(k - K - 2) is an
-        // exact f16 (no lower bit below 2^-24, at most 112): the block routine
-        // then runs on the values scaled by 2^-K (exact: powers of two), with
-        // S_enc and S_enc / 6 scaled by 2^K so that every rounding is the same.
-        uint32_t w4v[2], stv[2];
-        int kmax = -1000, kmin = 1000;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = 64 * hh + lane + 32 * h;
-            stv[h] = sm.trailer[s][r][0];
-            w4v[h] = *reinterpret_cast<const uint32_t *>(&sm.scales[s][r][4 * cq]);
-            const int k = (int)(stv[h] >> 23) - 127;
-            if (w4v[h] != 0u) {
-                kmax = max(kmax, k);
-                kmin = min(kmin, k);
-            }
-        }
+        // Decode-scale table of the warp's 16 rows and the strip's 16 column
+        // blocks: lane l builds row pair l & 7 (rows 16w + 2(l & 7), + 1) of
+        // the column blocks 4(l >> 3) .. + 3.  When the token exponents k of
+        // the rows with a nonzero scale lie within 13 of their maximum K,
+        // every s_b 2^(k - K - 2) is an exact f16 (no lower bit below 2^-24,
+        // at most 112): the table then holds, per column block and row pair,
+        // (w_a, w_b) and (w_a, -w_b) as f16 pairs (the RHT sign and the 1/4
+        // folded in), and the block arithmetic runs on the values scaled by
+        // 2^-K, with S_enc and S_enc / 6 scaled by 2^K (powers of two: every
+        // rounding is the same as unscaled).
+        const int rp = lane & 7, bq = lane >> 3;
+        const int ra0 = 16 * warp + 2 * rp, ra1 = ra0 + 1;
+        const uint32_t st0 = sm.trailer[s][ra0][0], st1 = sm.trailer[s][ra1][0];
+        const uint32_t w40 = *reinterpret_cast<const uint32_t *>(&sm.scales[s][ra0][4 * bq]);
+        const uint32_t w41 = *reinterpret_cast<const uint32_t *>(&sm.scales[s][ra1][4 * bq]);
+        const int k0 = (int)(st0 >> 23) - 127, k1 = (int)(st1 >> 23) - 127;
+        int kmax = max(w40 ? k0 : -1000, w41 ? k1 : -1000);
+        int kmin = min(w40 ? k0 : 1000, w41 ? k1 : 1000);
         kmax = __reduce_max_sync(0xffffffffu, kmax);
         kmin = __reduce_min_sync(0xffffffffu, kmin);
         const int K = kmax >= kmin ? kmax : 0;
         const float se16 = m.se * exp2i(K), ce16 = m.ce * exp2i(K);
         const bool f16 = kmin >= K - 13 && se16 >= 0x1p-100f && se16 <= 0x1p100f;
-        uint16_t(*t16)[kT16Stride] = reinterpret_cast<uint16_t(*)[kT16Stride]>(&tab[0][0]);
+        const bool neg0 = (p.sign_mask >> (2 * rp)) & 1u, neg1 = (p.sign_mask >> (2 * rp + 1)) & 1u;
+        if (f16) {
+            float f0 = w40 ? exp2i(k0 - K - 2) : 0.0f, f1 = w41 ? exp2i(k1 - K - 2) : 0.0f;
+            if (neg0)
+                f0 = -f0;
+            if (neg1)
+                f1 = -f1;
+            const uint32_t fp = cvt_f16x2(f0, f1);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int rloc = lane + 32 * h, r = 64 * hh + rloc;
-            const bool neg = (p.sign_mask >> (r & 15)) & 1u;
-            const uint32_t w4 = w4v[h];
-            const float2 a = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w4 & 0xffffu));
-            const float2 b = f16x2_to_f32x2(cvt_f16x2_from_e4m3x2(w4 >> 16));
-            if (f16) {
-                const int k = (int)(stv[h] >> 23) - 127;
-                float f = w4 != 0u ? exp2i(k - K - 2) : 0.0f;
-                if (neg)
-                    f = -f;
-                uint32_t lo, hi;
-                if (kSR) {
-                    // the same exact values as f16 products of exact f16
-                    // values (2^(k-K-2) in 2^[-15, -2], subnormal at -15):
-                    // fewer registers live in the SR kernel
-                    const uint32_t f2 = cvt_f16x2(f, f);
-                    lo = hmul2_rn(cvt_f16x2_from_e4m3x2(w4 & 0xffffu), f2);
-                    hi = hmul2_rn(cvt_f16x2_from_e4m3x2(w4 >> 16), f2);
-                } else {
-                    lo = cvt_f16x2(a.x * f, a.y * f);
-                    hi = cvt_f16x2(b.x * f, b.y * f);
-                }
-                t16[0][rloc] = (uint16_t)lo;
-                t16[1][rloc] = (uint16_t)(lo >> 16);
-                t16[2][rloc] = (uint16_t)hi;
-                t16[3][rloc] = (uint16_t)(hi >> 16);
-            } else {
-                float rs = u2f(stv[h]) * 0.25f;
-                if (neg)
-                    rs = -rs;
-                const float v0 = a.x * rs, v1 = a.y * rs, v2 = b.x * rs, v3 = b.y * rs;
-                tab[0][rloc] = make_float2(v0, v0);
-                tab[1][rloc] = make_float2(v1, v1);
-                tab[2][rloc] = make_float2(v2, v2);
-                tab[3][rloc] = make_float2(v3, v3);
+            for (int b = 0; b < 4; ++b) {
+                // (s_b of row a, s_b of row b) -> f16 pair, times (f_a, f_b): exact
+                const uint32_t sb = __byte_perm(w40, w41, (uint32_t)(b | ((b + 4) << 4)));
+                const uint32_t w2 = hmul2_rn(cvt_f16x2_from_e4m3x2(sb), fp);
+                sm.tab.t16[warp][4 * bq + b][rp] = make_uint2(w2, w2 ^ 0x80000000u);
             }
-        }
-        const float *rtab = sm.wrtab[warp];
-        // S_enc / s by a Markstein step on the f16 path; else from this warp's
-        // table of the expert's 128 quotients
-        if (!f16 && m.e != cur_e) {
-            cur_e = m.e;
+        } else {
+            float rs0 = u2f(st0) * 0.25f, rs1 = u2f(st1) * 0.25f;
+            if (neg0)
+                rs0 = -rs0;
+            if (neg1)
+                rs1 = -rs1;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int code = lane + 32 * q;
-                const float sv = e4m3_to_f32((uint32_t)code);
-                sm.wrtab[warp][code] = (sv == 0.0f) ? 0.0f : __fdiv_rn(m.se, sv);
+            for (int b = 0; b < 4; ++b) {
+                sm.tab.t32[warp][4 * bq + b][2 * rp] = e4m3_to_f32((w40 >> (8 * b)) & 0xffu) * rs0;
+                sm.tab.t32[warp][4 * bq + b][2 * rp + 1] = e4m3_to_f32((w41 >> (8 * b)) & 0xffu) * rs1;
             }
         }
         __syncwarp();
 
-        const int h0 = st * kTileCols + 2 * pc;
-        uint32_t csc0 = 0u, csc1 = 0u;
+        // columns h0 .. h0 + 7 (all inside H, which is a multiple of 32)
+        const int h0 = st * kTileCols + 8 * lane;
         if (h0 < H) {
-            const float2 *ctab = &tab[lane >> 3][0];
-            const uint32_t *c16 = reinterpret_cast<const uint32_t *>(&t16[lane >> 3][0]);
-            uint8_t *d0 = p.cw_codes + (int64_t)m.off * (H / 2) + (int64_t)h0 * (m.n / 2) + (rl + 64 * hh) / 2;
-            uint8_t *d1 = d0 + (m.n / 2);
-            uint32_t sc0 = 0u, sc1 = 0u;
-            uint4 q0[2], q1[2];   // 32 bytes (64 rows) of codes of columns h0 and h0 + 1
+            uint32_t cw[16];
 #pragma unroll
-            for (int bp = 0; bp < 2; ++bp) {
-                uint2 a0, a1, b0, b1;
-                uint32_t s2a, s2b;
-                const int r0 = 64 * hh + 32 * bp;
-                if (f16) {
-                    rht_block<kSR, true, true>(sm, s, c16 + 16 * bp, rtab, pc, r0, ce16, se16, p, m, h0, rl, a0, a1,
-                                               s2a);
-                    rht_block<kSR, true, true>(sm, s, c16 + 16 * bp + 8, rtab, pc, r0 + 16, ce16, se16, p, m, h0, rl,
-                                               b0, b1, s2b);
-                } else {
-                    rht_block<kSR, false, false>(sm, s, ctab + 32 * bp, rtab, pc, r0, m.ce, m.se, p, m, h0, rl, a0,
-                                                 a1, s2a);
-                    rht_block<kSR, false, false>(sm, s, ctab + 32 * bp + 16, rtab, pc, r0 + 16, m.ce, m.se, p, m, h0,
-                                                 rl, b0, b1, s2b);
+            for (int i = 0; i < 16; ++i)
+                cw[i] = *reinterpret_cast<const uint32_t *>(&sm.codes[s][16 * warp + i][4 * lane]);
+            // Philox counter of column h0, this row block: (off_e H + h0 n_e + row) / 16
+            const uint32_t nstep = (uint32_t)(m.n >> 4);
+            const uint64_t nbase = kSR ? ((uint64_t)m.off * (uint64_t)H + (uint64_t)h0 * (uint64_t)m.n +
+                                          (uint64_t)(rl + 16 * warp)) >> 4
+                                       : 0u;
+            float t32[16];
+            if (f16) {
+                uint2 t16[8];
+                const uint4 *tp = reinterpret_cast<const uint4 *>(&sm.tab.t16[warp][lane >> 1][0]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 v = tp[j];
+                    t16[2 * j] = make_uint2(v.x, v.y);
+                    t16[2 * j + 1] = make_uint2(v.z, v.w);
                 }
-                q0[bp] = make_uint4(a0.x, a0.y, b0.x, b0.y);
-                q1[bp] = make_uint4(a1.x, a1.y, b1.x, b1.y);
-                sc0 |= ((s2a & 0xffu) | ((s2b & 0xffu) << 8)) << (16 * bp);
-                sc1 |= (((s2a >> 8) & 0xffu) | (((s2b >> 8) & 0xffu) << 8)) << (16 * bp);
-            }
-            // one full 32-byte sector per column when the buffer allows it
-            if (p.cw_v8) {
-                st32g(d0, q0[0], q0[1]);
-                st32g(d1, q1[0], q1[1]);
+                rht_thread<kSR, true>(cw, t16, t32, sm.rcp, se16, ce16, p.key, nbase, nstep, outc, outs, lane);
             } else {
-                st16g(d0, q0[0]);
-                st16g(d0 + 16, q0[1]);
-                st16g(d1, q1[0]);
-                st16g(d1 + 16, q1[1]);
-            }
-            // tiled layout: this warp's 4 scale bytes of a column are one word
-            // of the expert's tile (column / 128, row-in-expert / 64)
-            if (kSwz) {
-                uint8_t *t = p.cw_scales + (int64_t)m.off * (H / 16) +
-                             ((int64_t)(h0 >> 7) * (m.n / 64) + (rl + 64 * hh) / 64) * 512 + ((h0 & 127) >> 5) * 4;
-                *reinterpret_cast<uint32_t *>(t + (h0 & 31) * 16) = sc0;
-                *reinterpret_cast<uint32_t *>(t + ((h0 + 1) & 31) * 16) = sc1;
-            }
-            // rows 64..127 hand their scale bytes to the warp holding rows
-            // 0..63 of the same columns, so each column's 8 scale bytes of
-            // the tile leave in one store (the stage's reuse orders the
-            // buffer: the producer refills stage s only after both warps
-            // released it)
-            else if (hh == 1) {
-                sm.csc[s][cq][lane][0] = sc0;
-                sm.csc[s][cq][lane][1] = sc1;
-            } else {
-                csc0 = sc0;
-                csc1 = sc1;
-            }
-        }
-        if (kSwz) {
-        } else if (hh == 1) {
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&sm.csc_full[s][cq]);
-        } else {
-            if (!mbar_wait_bounded(&sm.csc_full[s][cq], ph)) {
-                if (lane == 0) {
-                    sm.abort_flag = 1;
-                    raise_status(p.status, kDevErrTimeout);
+                const float4 *tp = reinterpret_cast<const float4 *>(&sm.tab.t32[warp][lane >> 1][0]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 v = tp[j];
+                    t32[4 * j] = v.x;
+                    t32[4 * j + 1] = v.y;
+                    t32[4 * j + 2] = v.z;
+                    t32[4 * j + 3] = v.w;
                 }
-                break;
-            }
-            if (h0 < H) {
-                uint8_t *cs = p.cw_scales + (int64_t)m.off * (H / 16) + (int64_t)h0 * (m.n / 16) + rl / 16;
-                *reinterpret_cast<uint2 *>(cs) = make_uint2(csc0, sm.csc[s][cq][lane][0]);
-                *reinterpret_cast<uint2 *>(cs + m.n / 16) = make_uint2(csc1, sm.csc[s][cq][lane][1]);
+                rht_thread_f32<kSR>(cw, t32, sm.rcp, m.se, m.ce, p.key, nbase, nstep, outc, outs, lane);
             }
         }
 
-        // release the stage (after the rowwise TMA store has read it); the
+        // release the stage (the rowwise TMA store having read it); the
         // last warp to release it refills it with the tile kStages ahead
         if (c == 0 && p.do_rowwise)
             tma_store_wait_read0();
@@ -597,6 +610,63 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
                     mbar_arrive(&sm.full[s]);
                     atomicAdd(&sm.issued, 1);
                 }
+            }
+            // this warp's staging of the tile is written
+            mbar_arrive(&sm.stg_full[par]);
+        }
+        // all 8 row blocks staged (the other parity's buffer is the next
+        // tile's: every thread finished reading it before its warp arrived
+        // here)
+        if (!mbar_wait_bounded(&sm.stg_full[par], (uint32_t)(it >> 1) & 1u) || sm.abort_flag) {
+            if (lane == 0) {
+                sm.abort_flag = 1;
+                raise_status(p.status, kDevErrTimeout);
+            }
+            break;
+        }
+
+        // stores: thread c takes column h = 256 st + c: its 64 code bytes (two
+        // full sectors of the [H][n_e / 2] layout) and its 8 scale bytes
+        const int h = st * kTileCols + c;
+        if (h < H) {
+            const int l = c >> 3, pp = (c >> 1) & 3, half = c & 1;
+            const int off8 = stage_off(l, pp) + 8 * half;
+            uint32_t v[16];
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const uint2 x = *reinterpret_cast<const uint2 *>(&sm.outc[par][w][off8]);
+                v[2 * w] = x.x;
+                v[2 * w + 1] = x.y;
+            }
+            uint8_t *d = p.cw_codes + (int64_t)m.off * (H / 2) + (int64_t)h * (m.n / 2) + rl / 2;
+            if (p.cw_v8) {
+                st32g(d, make_uint4(v[0], v[1], v[2], v[3]), make_uint4(v[4], v[5], v[6], v[7]));
+                st32g(d + 32, make_uint4(v[8], v[9], v[10], v[11]), make_uint4(v[12], v[13], v[14], v[15]));
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st16g(d + 16 * q, make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+            }
+            // scale byte of row block w is byte (c & 3) of word c >> 2 of warp w's area
+            uint32_t sw[8];
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+                sw[w] = reinterpret_cast<const uint32_t *>(sm.outs[par][w])[c >> 2];
+            const uint32_t sel = (uint32_t)(c & 3) * 0x11u;          // byte c & 3 of each word
+            const uint32_t lo = __byte_perm(__byte_perm(sw[0], sw[1], sel | 0x0040u) & 0xffffu,
+                                            __byte_perm(sw[2], sw[3], sel | 0x0040u), 0x5410);
+            const uint32_t hi = __byte_perm(__byte_perm(sw[4], sw[5], sel | 0x0040u) & 0xffffu,
+                                            __byte_perm(sw[6], sw[7], sel | 0x0040u), 0x5410);
+            if (kSwz) {
+                // tiled layout: the 4 scale bytes of a column's 64 rows are one
+                // word of the expert's tile (column / 128, row-in-expert / 64)
+                uint8_t *tt = p.cw_scales + (int64_t)m.off * (H / 16) + ((int64_t)(h >> 7) * (m.n / 64) + rl / 64) * 512 +
+                              ((h & 127) >> 5) * 4 + (h & 31) * 16;
+                *reinterpret_cast<uint32_t *>(tt) = lo;
+                *reinterpret_cast<uint32_t *>(tt + 512) = hi;
+            } else {
+                uint8_t *cs = p.cw_scales + (int64_t)m.off * (H / 16) + (int64_t)h * (m.n / 16) + rl / 16;
+                *reinterpret_cast<uint2 *>(cs) = make_uint2(lo, hi);
             }
         }
         done = it + 1;
@@ -624,9 +694,9 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         for (int i = 0; i < Sm::kNS; ++i) {
             mbar_init(&sm.full[i], 1);
             sm.rel[i] = 0u;
-            for (int q = 0; q < kConsumerWarps / 2; ++q)
-                mbar_init(&sm.csc_full[i][q], 1);
         }
+        mbar_init(&sm.stg_full[0], kConsumerWarps);
+        mbar_init(&sm.stg_full[1], kConsumerWarps);
         sm.abort_flag = 0;
         sm.consumed = 0x7fffffff;
         fence_mbar_init();
@@ -653,11 +723,11 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     pdl_launch_dependents();
 
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x)
-        sm.offs[i] = __ldg(p.offsets + i);
+        smem_offs(sm)[i] = __ldg(p.offsets + i);
     for (int i = threadIdx.x; i < 128; i += blockDim.x)
         sm.rcp[i] = p.rcp[i];
     __syncthreads();
-    int R = sm.offs[p.E];
+    int R = smem_offs(sm)[p.E];
     if (R > p.R_cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0)
             raise_status(p.status, kDevErrCapacity);
@@ -675,7 +745,7 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
             const float a = p.amax_in[i];
             float ac;
             const float se = colwise_encode_scale(a, ac);
-            sm.se_cache[i] = se;
+            smem_se(sm, p.E)[i] = se;
             if (blockIdx.x == 0) {
                 p.amax_row[i] = a;
                 p.amax_col[i] = ac;
@@ -684,7 +754,7 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         }
     } else {
         for (int i = threadIdx.x; i < p.E; i += blockDim.x)
-            sm.se_cache[i] = p.scale_enc[i];
+            smem_se(sm, p.E)[i] = p.scale_enc[i];
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -817,11 +887,14 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
     }
 
     const bool sr = rounding == 1;
-    const size_t smem = (sr ? sizeof(DrCfg<true>::Smem) : sizeof(DrCfg<false>::Smem)) + 1024;
+    const size_t smem_fixed = (sr ? sizeof(DrCfg<true>::Smem) : sizeof(DrCfg<false>::Smem)) + 1024;
+    const size_t smem = smem_fixed + (size_t)(2 * E + 1) * 4;
     static std::atomic<uint32_t> done[4][2] = {};
     auto kern = sr ? (swz ? direct_receive_kernel<true, true> : direct_receive_kernel<true, false>)
                    : (swz ? direct_receive_kernel<false, true> : direct_receive_kernel<false, false>);
-    err = ensure_smem_limit(kern, c.device, (int)smem, done[(sr ? 2 : 0) + (swz ? 1 : 0)]);
+    // the limit is set once per device, for the largest expert count
+    err = ensure_smem_limit(kern, c.device, (int)(smem_fixed + (2 * kMaxExperts + 1) * 4),
+                            done[(sr ? 2 : 0) + (swz ? 1 : 0)]);
     if (err != cudaSuccess)
         return err;
     const int64_t max_units = (int64_t)(R_cap / kTileRows) * a.n_strips;
