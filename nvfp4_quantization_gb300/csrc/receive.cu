@@ -83,6 +83,7 @@ struct __align__(128) DrSmem {
     StageMeta meta[NS];
     uint64_t full[NS];
     uint64_t stg_full[2];                       // outc / outs [parity] written by all 8 warps
+    uint64_t stg_empty[2];                      // outc / outs [parity] read (stored) by all 8 warps
     uint32_t rel[NS];                      // warps done with the stage's current tile
     int abort_flag;
     int consumed;                               // fewest tiles any warp finished
@@ -430,13 +431,82 @@ __device__ __noinline__ void rht_thread_f32(const uint32_t (&cw)[16], const floa
     rht_thread<kSR, false>(cw, t16, t32, rcp, se, ce, K, nbase, nstep, outc, outs, lane);
 }
 
+// The store phase of one staged tile (expert slot at row `off`, n rows;
+// rows rl .. rl + 127 of the expert; strip st): thread c takes column
+// h = 256 st + c, its 64 code bytes (two full sectors of the [H][n_e / 2]
+// layout) and its 8 scale bytes.
+template <bool kSwz, class Sm>
+__device__ __forceinline__ void store_tile(const Sm &sm, const DrArgs &p, int par, int off, int n, int rl, int st)
+{
+    const int c = threadIdx.x, H = p.H;
+    const int h = st * kTileCols + c;
+    if (h >= H)
+        return;
+    const int l = c >> 3, pp = (c >> 1) & 3, half = c & 1;
+    const int off8 = stage_off(l, pp) + 8 * half;
+    uint32_t v[16];
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+        const uint2 x = *reinterpret_cast<const uint2 *>(&sm.outc[par][w][off8]);
+        v[2 * w] = x.x;
+        v[2 * w + 1] = x.y;
+    }
+    uint8_t *d = p.cw_codes + (int64_t)off * (H / 2) + (int64_t)h * (n / 2) + rl / 2;
+    if (p.cw_v8) {
+        st32g(d, make_uint4(v[0], v[1], v[2], v[3]), make_uint4(v[4], v[5], v[6], v[7]));
+        st32g(d + 32, make_uint4(v[8], v[9], v[10], v[11]), make_uint4(v[12], v[13], v[14], v[15]));
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            st16g(d + 16 * q, make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    }
+    // scale byte of row block w is byte (c & 3) of word c >> 2 of warp w's area
+    uint32_t sw[8];
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w)
+        sw[w] = reinterpret_cast<const uint32_t *>(sm.outs[par][w])[c >> 2];
+    const uint32_t sel = (uint32_t)(c & 3) * 0x11u | 0x0040u;   // byte c & 3 of two words
+    const uint32_t lo = __byte_perm(__byte_perm(sw[0], sw[1], sel) & 0xffffu, __byte_perm(sw[2], sw[3], sel), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(sw[4], sw[5], sel) & 0xffffu, __byte_perm(sw[6], sw[7], sel), 0x5410);
+    if (kSwz) {
+        // tiled layout: the 4 scale bytes of a column's 64 rows are one word
+        // of the expert's tile (column / 128, row-in-expert / 64)
+        uint8_t *tt = p.cw_scales + (int64_t)off * (H / 16) + ((int64_t)(h >> 7) * (n / 64) + rl / 64) * 512 +
+                      ((h & 127) >> 5) * 4 + (h & 31) * 16;
+        *reinterpret_cast<uint32_t *>(tt) = lo;
+        *reinterpret_cast<uint32_t *>(tt + 512) = hi;
+    } else {
+        uint8_t *cs = p.cw_scales + (int64_t)off * (H / 16) + (int64_t)h * (n / 16) + rl / 16;
+        *reinterpret_cast<uint2 *>(cs) = make_uint2(lo, hi);
+    }
+}
+
+// A bounded wait on phase `k & 1` of a staging barrier; false (with the
+// abort flag and the timeout status set) if it gave up or another warp has.
+template <class Sm>
+__device__ __forceinline__ bool stage_wait(Sm &sm, uint64_t *bar, int k, const DrArgs &p)
+{
+    if (mbar_wait_bounded(bar, (uint32_t)k & 1u) && !sm.abort_flag)
+        return true;
+    if ((threadIdx.x & 31) == 0) {
+        sm.abort_flag = 1;
+        raise_status(p.status, kDevErrTimeout);
+    }
+    return false;
+}
+
 // Warp w computes row block w (rows 16w .. 16w + 15) of the tile, lane l the
 // columns 8l .. 8l + 7 of the strip (the code bytes 4l .. 4l + 3 of each row:
 // a warp's loads cover whole 128-byte rows).  A column's 128 rows thus come
 // from all 8 warps: each warp stages its 8 code bytes and one scale byte per
-// column, the 8 warps meet at an mbarrier (double-buffered staging, so once
-// per tile), and thread c then stores column c's 64 code bytes (two full
-// sectors) and 8 scale bytes.
+// column (two staging buffers, used by alternate tiles), and thread c stores
+// column c's 64 code bytes (two full sectors) and 8 scale bytes once all 8
+// warps have staged the tile.  That store phase of a tile runs after the
+// warp's compute of the next one, so the warps reach it at different times:
+// the stores do not leave in one burst, and a warp waits only for the
+// slowest warp of the tile before.  Per buffer, stg_full counts the 8 warps'
+// stagings and stg_empty their store phases (a buffer is written again two
+// tiles later, after every warp has stored from it).
 template <bool kSR, bool kSwz, class Sm>
 __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, const CUtensorMap *tm_rws,
                                              const CUtensorMap *tmc, const CUtensorMap *tms,
@@ -446,6 +516,8 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
     const int warp = c >> 5, lane = c & 31;
     const int H = p.H;
     int done = 0;
+    bool ok = true;
+    int prev_off = 0, prev_n = 0, prev_rl = 0, prev_st = 0;   // the tile before, staged, not yet stored
     int rt, st;
     for (int it = 0; tile_of(p, n_units, it, rt, st); ++it) {
         const int s = it % Sm::kNS;
@@ -455,6 +527,7 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
                 sm.abort_flag = 1;
                 raise_status(p.status, kDevErrTimeout);
             }
+            ok = false;
             break;
         }
         const StageMeta m = sm.meta[s];
@@ -551,6 +624,12 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
         }
         __syncwarp();
 
+        // this tile's staging buffer was last read by the store phase of the
+        // tile two before
+        if (it >= 2 && !stage_wait(sm, &sm.stg_empty[par], (it - 2) >> 1, p)) {
+            ok = false;
+            break;
+        }
         // columns h0 .. h0 + 7 (all inside H, which is a multiple of 32)
         const int h0 = st * kTileCols + 8 * lane;
         if (h0 < H) {
@@ -614,63 +693,26 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
             // this warp's staging of the tile is written
             mbar_arrive(&sm.stg_full[par]);
         }
-        // all 8 row blocks staged (the other parity's buffer is the next
-        // tile's: every thread finished reading it before its warp arrived
-        // here)
-        if (!mbar_wait_bounded(&sm.stg_full[par], (uint32_t)(it >> 1) & 1u) || sm.abort_flag) {
-            if (lane == 0) {
-                sm.abort_flag = 1;
-                raise_status(p.status, kDevErrTimeout);
+        // the tile before: once all 8 warps staged it, store it and free its buffer
+        if (it >= 1) {
+            if (!stage_wait(sm, &sm.stg_full[par ^ 1], (it - 1) >> 1, p)) {
+                ok = false;
+                break;
             }
-            break;
+            store_tile<kSwz>(sm, p, par ^ 1, prev_off, prev_n, prev_rl, prev_st);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.stg_empty[par ^ 1]);
         }
-
-        // stores: thread c takes column h = 256 st + c: its 64 code bytes (two
-        // full sectors of the [H][n_e / 2] layout) and its 8 scale bytes
-        const int h = st * kTileCols + c;
-        if (h < H) {
-            const int l = c >> 3, pp = (c >> 1) & 3, half = c & 1;
-            const int off8 = stage_off(l, pp) + 8 * half;
-            uint32_t v[16];
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const uint2 x = *reinterpret_cast<const uint2 *>(&sm.outc[par][w][off8]);
-                v[2 * w] = x.x;
-                v[2 * w + 1] = x.y;
-            }
-            uint8_t *d = p.cw_codes + (int64_t)m.off * (H / 2) + (int64_t)h * (m.n / 2) + rl / 2;
-            if (p.cw_v8) {
-                st32g(d, make_uint4(v[0], v[1], v[2], v[3]), make_uint4(v[4], v[5], v[6], v[7]));
-                st32g(d + 32, make_uint4(v[8], v[9], v[10], v[11]), make_uint4(v[12], v[13], v[14], v[15]));
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st16g(d + 16 * q, make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
-            }
-            // scale byte of row block w is byte (c & 3) of word c >> 2 of warp w's area
-            uint32_t sw[8];
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                sw[w] = reinterpret_cast<const uint32_t *>(sm.outs[par][w])[c >> 2];
-            const uint32_t sel = (uint32_t)(c & 3) * 0x11u;          // byte c & 3 of each word
-            const uint32_t lo = __byte_perm(__byte_perm(sw[0], sw[1], sel | 0x0040u) & 0xffffu,
-                                            __byte_perm(sw[2], sw[3], sel | 0x0040u), 0x5410);
-            const uint32_t hi = __byte_perm(__byte_perm(sw[4], sw[5], sel | 0x0040u) & 0xffffu,
-                                            __byte_perm(sw[6], sw[7], sel | 0x0040u), 0x5410);
-            if (kSwz) {
-                // tiled layout: the 4 scale bytes of a column's 64 rows are one
-                // word of the expert's tile (column / 128, row-in-expert / 64)
-                uint8_t *tt = p.cw_scales + (int64_t)m.off * (H / 16) + ((int64_t)(h >> 7) * (m.n / 64) + rl / 64) * 512 +
-                              ((h & 127) >> 5) * 4 + (h & 31) * 16;
-                *reinterpret_cast<uint32_t *>(tt) = lo;
-                *reinterpret_cast<uint32_t *>(tt + 512) = hi;
-            } else {
-                uint8_t *cs = p.cw_scales + (int64_t)m.off * (H / 16) + (int64_t)h * (m.n / 16) + rl / 16;
-                *reinterpret_cast<uint2 *>(cs) = make_uint2(lo, hi);
-            }
-        }
+        prev_off = m.off;
+        prev_n = m.n;
+        prev_rl = rl;
+        prev_st = st;
         done = it + 1;
     }
+    // the last tile
+    if (ok && done >= 1 && stage_wait(sm, &sm.stg_full[(done - 1) & 1], (done - 1) >> 1, p))
+        store_tile<kSwz>(sm, p, (done - 1) & 1, prev_off, prev_n, prev_rl, prev_st);
     if (c == 0 && p.do_rowwise)
         tma_store_wait0();
     return done;
@@ -697,6 +739,8 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
         }
         mbar_init(&sm.stg_full[0], kConsumerWarps);
         mbar_init(&sm.stg_full[1], kConsumerWarps);
+        mbar_init(&sm.stg_empty[0], kConsumerWarps);
+        mbar_init(&sm.stg_empty[1], kConsumerWarps);
         sm.abort_flag = 0;
         sm.consumed = 0x7fffffff;
         fence_mbar_init();
