@@ -218,14 +218,14 @@ DR_SOURCES = ["nvfp4_quantization_gb300/csrc/receive.cu", "nvfp4_quantization_gb
 
 
 def profiled_traffic(kernel: str, sources, config: int) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source and on this workload; else None."""
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, if it was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        rec = d[kernel]
-        if rec.get("source_sha") != source_sha(sources) or rec.get("config") != config:
+        rec = d[kernel][str(int(config))]
+        if rec.get("source_sha") != source_sha(sources):
             return None
         return float(rec["dram_bytes_per_launch"])
     except Exception:
