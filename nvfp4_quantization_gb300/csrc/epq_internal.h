@@ -116,6 +116,12 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
                                   int rounding, uint64_t seed, uint32_t sign_mask,
                                   uint32_t *status, bool swz = false, const float *amax_in = nullptr);
 
+// Tensor map of a 2-D byte tensor [outer][inner] with a row pitch of `pitch`
+// bytes and a box of box_outer rows x box_inner bytes (no swizzle, L2
+// promotion 256 B); false if the driver refuses it.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t pitch,
+              uint32_t box_inner, uint32_t box_outer);
+
 // Bytes of a packed NVFP4 row: roundup16(9H/16 + 16).
 inline int64_t row_bytes(int64_t H) { return (9 * H / 16 + 16 + 15) / 16 * 16; }
 

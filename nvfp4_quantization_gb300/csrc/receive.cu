@@ -854,7 +854,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // 2-D byte tensor [outer][inner] with a row pitch of `pitch` bytes.
-static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t pitch,
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t pitch,
                      uint32_t box_inner, uint32_t box_outer)
 {
     auto enc = tensor_map_encoder();

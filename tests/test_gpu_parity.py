@@ -350,7 +350,8 @@ def grouped_bf16_rows(w, R_cap):
     return x, off, amax
 
 
-@pytest.mark.parametrize("name,scale", [("cfg2", 1.0), ("cfg4", 1.0), ("cfg4_ragged_H", 1.0), ("cfg2", 3.3)])
+@pytest.mark.parametrize("name,scale", [("cfg2", 1.0), ("cfg4", 1.0), ("cfg4_ragged_H", 1.0), ("cfg1_ragged_H", 1.0),
+                                        ("cfg2", 3.3)])
 def test_parity_colwise_rht_bf16(name, scale):
     """ep_nvfp4_colwise_rht_bf16 (the supplied-amax path) against the oracle,
     byte for byte; the supplied amax is the input's own (as the dGLU epilogue
