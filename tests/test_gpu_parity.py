@@ -333,6 +333,28 @@ def test_route_plan_small_batch_shapes(T, E, k):
     assert int(plan.status.item()) == st
 
 
+@pytest.mark.parametrize("T,E,k", [(9000, 700, 8), (16384, 256, 8), (12000, 64, 6), (16384, 752, 2),
+                                   (16384, 760, 3)])
+def test_route_plan_large_batches(T, E, k):
+    """Batches of 8193 to 16384 tokens (more 512-token chunks than one
+    thread-block cluster holds) with up to 760 experts, with dropped,
+    out-of-range and repeated ids."""
+    rng = np.random.default_rng(T + 13 * E + k)
+    topk = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    topk[rng.random((T, k)) < 0.03] = -1
+    topk[rng.random((T, k)) < 0.002] = -7
+    if k > 1:
+        rep = rng.random(T) < 0.01
+        topk[rep, k - 1] = topk[rep, 0]
+    off, cnt, dest, st = oracle.route_plan(topk, E, 128)
+    plan = nq.ep_route_plan(torch.from_numpy(topk).cuda(), E, 128)
+    torch.cuda.synchronize()
+    assert_bytes_equal(plan.offsets.cpu().numpy(), off, "offsets")
+    assert_bytes_equal(plan.counts.cpu().numpy(), cnt, "counts")
+    assert_bytes_equal(plan.dest.cpu().numpy()[: T * k], dest, "dest")
+    assert int(plan.status.item()) == st != 0
+
+
 def grouped_bf16_rows(w, R_cap):
     """Expert-grouped BF16 rows [R_cap, H] of a workload (token t at each of
     its destination rows, padding rows zero) and the exact per-expert amax."""
