@@ -263,7 +263,8 @@ typedef struct {
  * that measures the amax; TE PR #3755, PR description: after the RHT no
  * columnwise value exceeds four times the rowwise amax; TE PR #3324,
  * description: NVFP4 operands with one FP32 scale per row (per token).
- *   rows            device u8 [R_cap, S].
+ *   rows            device u8 [R_cap, S]; R_cap * H above 2^36 (element
+ *                   positions of 36 bits or more) -> EP_ERR_CAPACITY.
  *   expert_amax     device f32 [E] or NULL: each expert's amax, the largest
  *                   token amax A_t over its rows, already reduced (as
  *                   ep_nvfp4_pack / ep_nvfp4_dispatch leave it); the outputs

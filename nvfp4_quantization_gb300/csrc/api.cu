@@ -336,7 +336,8 @@ static ep_status direct_receive_common(const uint8_t *rows, int64_t R_cap, int64
         return EP_ERR_NULL;
     if (!shape_ok(0, H, 1, E) || (swz && H % 128 != 0))
         return EP_ERR_SHAPE;
-    if (R_cap < 0 || R_cap > (int64_t)INT32_MAX)
+    // element positions (the SR counters) below 2^36
+    if (R_cap < 0 || R_cap > (int64_t)INT32_MAX || R_cap * H > ((int64_t)1 << 36))
         return EP_ERR_CAPACITY;
     if (rounding != EP_ROUND_RNE && rounding != EP_ROUND_SR)
         return EP_ERR_ARG;

@@ -128,8 +128,8 @@ __device__ __forceinline__ void cb_block(const uint32_t *w, uint32_t sign_mask, 
         u[i] = mul2(u[i], r2);
     if (kSR) {
         // rows 4q .. 4q + 3 of the block take word q of its column's Philox output (stream 2)
-        const Philox4 ra = sr_bytes16(key, 2u, pos);
-        const Philox4 rb = sr_bytes16(key, 2u, pos + (uint64_t)n);
+        const Philox4 ra = sr_bytes16_36(key, 2u, pos);
+        const Philox4 rb = sr_bytes16_36(key, 2u, pos + (uint64_t)n);
         c0 = make_uint2(cvt_e2m1x8_sr(u[0].x, u[1].x, u[2].x, u[3].x, u[4].x, u[5].x, u[6].x, u[7].x, ra.x, ra.y),
                         cvt_e2m1x8_sr(u[8].x, u[9].x, u[10].x, u[11].x, u[12].x, u[13].x, u[14].x, u[15].x, ra.z,
                                       ra.w));

@@ -436,6 +436,15 @@ __device__ __forceinline__ Philox4 sr_bytes16(const PhiloxKey &K, uint32_t strea
     return philox4x32_10((uint32_t)n, (uint32_t)(n >> 32), stream, 0u, K);
 }
 
+// sr_bytes16 for an element index below 2^36 (the grouped operands: offsets,
+// columns and rows address at most R_cap * H < 2^36 elements), whose counter's
+// second word is 0.  With that word a literal, the product of round 2 that
+// involves only the key is loop-invariant: 18 wide products per call, not 19.
+__device__ __forceinline__ Philox4 sr_bytes16_36(const PhiloxKey &K, uint32_t stream, uint64_t idx0)
+{
+    return philox4x32_10((uint32_t)(idx0 >> 4), 0u, stream, 0u, K);
+}
+
 // Eight FP32 values -> one word of eight E2M1 codes by stochastic rounding,
 // a[0] in the lowest nibble; a[0..3] take the random word r_lo, a[4..7] r_hi.
 // Within a word with bytes b0..b3 (b0 least significant), A = b2:b0 and

@@ -383,12 +383,14 @@ __device__ __forceinline__ void rht_pair(const uint32_t (&cw)[16], const uint2 (
 }
 
 // The Philox outputs of columns h and h + 1 of one 16-row block: counters
-// n and n + nstep (n = (off_e H + h n_e + row) / 16, nstep = n_e / 16).
+// n and n + nstep (n = (off_e H + h n_e + row) / 16, nstep = n_e / 16).  The
+// counter's second word, n / 2^32, is 0: the call's element positions are
+// below R_cap * H < 2^36 (the boundary refuses larger buffers).
 __device__ __forceinline__ void pair_random(const PhiloxKey &K, uint64_t n, uint32_t nstep, Philox4 &ra, Philox4 &rb)
 {
     const uint64_t n1 = n + nstep;
-    ra = philox4x32_10((uint32_t)n, (uint32_t)(n >> 32), 1u, 0u, K);
-    rb = philox4x32_10((uint32_t)n1, (uint32_t)(n1 >> 32), 1u, 0u, K);
+    ra = philox4x32_10((uint32_t)n, 0u, 1u, 0u, K);
+    rb = philox4x32_10((uint32_t)n1, 0u, 1u, 0u, K);
 }
 
 // The thread's four column pairs (8 columns x 16 rows).  With stochastic

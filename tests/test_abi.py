@@ -125,6 +125,12 @@ def test_receive_and_unpack_validation():
     g.rw_codes = None
     assert L.ep_nvfp4_direct_receive(FAKE, 128, 1000, FAKE, 4, None, ctypes.byref(g), 0, 0, 0, FAKE, None) == -2
     assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, None, ctypes.byref(g), 7, 0, 0, FAKE, None) == -5
+    # element positions (the stochastic-rounding counters) must stay below 2^36
+    assert L.ep_nvfp4_direct_receive(FAKE, 1 << 26, 1024, FAKE, 4, None, ctypes.byref(g), 0, 0, 0, FAKE, None) != -4
+    assert L.ep_nvfp4_direct_receive(FAKE, (1 << 26) + 1, 1024, FAKE, 4, None, ctypes.byref(g), 0, 0, 0, FAKE,
+                                     None) == -4
+    assert L.ep_nvfp4_direct_receive_swizzled(FAKE, (1 << 26) + 1, 1024, FAKE, 4, None, ctypes.byref(g), 0, 0, 0,
+                                              FAKE, None) == -4
     # a supplied per-expert amax must be 4-byte aligned
     bad = ctypes.c_void_p(0x10002)
     assert L.ep_nvfp4_direct_receive(FAKE, 128, 1024, FAKE, 4, bad, ctypes.byref(g), 0, 0, 0, FAKE, None) == -3
