@@ -756,11 +756,15 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     // amax kernel (only S_enc comes from it), and even before the expert
     // offsets are read: tile 0 of this CTA is loaded if it lies inside the
     // row capacity, and dropped unused if it lies past the rows in use.
-    // The other stages are loaded once it has arrived, so that at start-up,
-    // when every CTA asks at once, first tiles are not queued behind second
-    // ones.
     // With the amax supplied (p.amax_in) the grid before this one is the pack
     // itself, and no row may be read before the wait on it.
+    // The other stages' tiles are issued by lane 0 of warps 1 .. kStages - 1,
+    // one each, as soon as their rows may be read: the issue of a tile's
+    // three boxes holds its thread for a while, and done by thread 0 after
+    // tile 0 had arrived it kept warp 0 (and with it the whole tile) from
+    // starting.  Their bytes are expected on the stages' barriers at the
+    // issue; thread 0 writes the metadata and arrives (releasing both) after
+    // the barrier that follows S_enc.
     const int rt0 = (int)blockIdx.x / p.n_strips, st0 = (int)blockIdx.x % p.n_strips;
     const int pre = rt0 < p.R_cap / kTileRows ? 1 : 0;
     if (threadIdx.x == 0 && pre && !p.amax_in)
@@ -781,10 +785,17 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
     const int n_units = (R / kTileRows) * p.n_strips;
     const bool use0 = (int)blockIdx.x < n_units;   // tile 0 holds rows in use
+    const int wn = (int)threadIdx.x >> 5;            // the stage whose tile this thread issues
+    int rtn = 0, stn = 0;
+    const bool issuer = (threadIdx.x & 31) == 0 && wn >= 1 && wn < Sm::kNS && tile_of(p, n_units, wn, rtn, stn);
+    if (issuer && !p.amax_in)
+        issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, wn, rtn, stn);
 
     pdl_wait();
     if (threadIdx.x == 0 && pre && p.amax_in)
         issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, 0, rt0, st0);
+    if (issuer && p.amax_in)
+        issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, wn, rtn, stn);
     if (p.amax_in) {
         // S_enc of every expert from the supplied amax; CTA 0 writes the metadata
         for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
@@ -804,28 +815,24 @@ direct_receive_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        // metadata of tile 0; the arrival releases it (a dropped tile's
-        // arrival only lets its bytes be waited for before the exit)
+        // metadata of the first stages' tiles; each arrival releases its
+        // stage (a dropped tile 0's arrival only lets its bytes be waited
+        // for before the exit)
+        int issued = pre;
         if (pre) {
             if (use0)
                 stage_meta(sm, p, 0, rt0);
             mbar_arrive(&sm.full[0]);
-        }
-        sm.issued = pre;
-        // once the first tile is here, load the other stages (metadata, bytes
-        // expected, then the arrival that releases both); a wait that gives
-        // up is seen again, and handled, by the tile loop
-        if (pre && use0 && mbar_wait_bounded(&sm.full[0], 0u)) {
             for (int n = 1; n < Sm::kNS; ++n) {
                 int rt, st;
                 if (!tile_of(p, n_units, n, rt, st))
                     break;
                 stage_meta(sm, p, n, rt);
-                issue_tile(sm, &tm_codes, &tm_scales, &tm_trailer, n, rt, st);
                 mbar_arrive(&sm.full[n]);
-                sm.issued = n + 1;
+                issued = n + 1;
             }
         }
+        sm.issued = issued;
     }
 
     const int done = consumer_loop<kSR, kSwz>(sm, &tm_rw, &tm_rws, &tm_codes, &tm_scales, &tm_trailer, p, n_units);
