@@ -636,7 +636,19 @@ mxfp8_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
             const float2 bb = mul2(make_float2(bf16lo(w[2 * i + 1]), bf16hi(w[2 * i + 1])), f2);
             o[i] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(bb.x, bb.y) << 16);
         }
-        const uint8_t sbyte = (uint8_t)(e + 127);
+        const uint32_t sbyte = (uint32_t)(e + 127);
+        // the scale bytes of four neighbouring blocks (lanes 4i .. 4i + 3 of
+        // a warp) leave as one word when a row's scales are a whole number of
+        // words; the four lanes of a group are then all present (the block
+        // size is a multiple of 32 and q < nq holds for all four or none),
+        // and only they take part in the exchange
+        const bool wordwise = (nq & 3) == 0;
+        uint32_t sw = sbyte << (8 * (q & 3));
+        if (wordwise) {
+            const uint32_t grp = 0xfu << (threadIdx.x & 28u);
+            sw |= __shfl_xor_sync(grp, sw, 1);
+            sw |= __shfl_xor_sync(grp, sw, 2);
+        }
         for (int j = 0; j < k; ++j) {
             const int d = sdest[j];
             if (d < 0)
@@ -648,7 +660,10 @@ mxfp8_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
             uint8_t *row = buf + (int64_t)d * H + (int64_t)q * 32;
             st16(row, make_uint4(o[0], o[1], o[2], o[3]));
             st16(row + 16, make_uint4(o[4], o[5], o[6], o[7]));
-            scales[(int64_t)d * (H / 32) + q] = sbyte;
+            if (!wordwise)
+                scales[(int64_t)d * (H / 32) + q] = (uint8_t)sbyte;
+            else if ((q & 3) == 0)
+                *reinterpret_cast<uint32_t *>(scales + (int64_t)d * (H / 32) + q) = sw;
         }
     }
 }
