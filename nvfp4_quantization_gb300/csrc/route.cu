@@ -9,7 +9,8 @@
 //  1. each CTA takes a contiguous run of 512-token chunks (one thread per
 //     token), validates the ids and ranks every slot among the CTA's earlier
 //     slots of the same expert: per chunk, each warp owns one 32-bit word of
-//     every expert's token mask (filled with __match_any_sync, no atomics),
+//     every expert's token mask (each lane ORs its bit into the word of its
+//     slot's expert, a shared-memory atomic; no warp-synchronous match),
 //     the words are prefix-counted, and a running per-expert count carries
 //     over to the next chunk; the CTA's per-expert totals go to the workspace.
 //  2. after the barrier every CTA sums the totals of the CTAs before it (its
@@ -34,6 +35,13 @@ namespace epq {
 
 constexpr int kChunk = 512;              // tokens per chunk, one thread each
 constexpr int kWords = kChunk / 32;      // mask words per expert
+
+// The token masks live as [word][expert] rows of an odd pitch (E, or E + 1
+// when E is even): the 16 words of one expert (the per-expert prefix) fall on
+// 16 different banks, and the lanes of a warp looking up their own experts'
+// word `warp` collide only where two experts meet modulo 32 (with [expert]
+// [word] rows, every expert's word `warp` lay on one of two banks).
+__host__ __device__ inline int mask_pitch(int E) { return E | 1; }
 constexpr int kRankBits = 21;            // temp encoding: expert << 21 | rank in CTA
 constexpr int kWsHeader = 4;             // workspace words before the totals: barrier count, generation
 
@@ -132,7 +140,7 @@ constexpr int kMaxClusterCtas = 16;   // largest (non-portable) thread-block clu
 // barrier and phase 2 reads the other CTAs' totals through distributed shared
 // memory, so no global round trip separates the phases.
 template <bool kCluster>
-__global__ void __launch_bounds__(kChunk)
+__global__ void __launch_bounds__(kChunk, 1)
 route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A,
                       int32_t *__restrict__ offsets, int32_t *__restrict__ counts, int32_t *__restrict__ dest,
                       uint32_t *__restrict__ ws, uint32_t *__restrict__ status, float *__restrict__ amax_zero)
@@ -142,9 +150,10 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
     if (amax_zero && blockIdx.x == 0)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             amax_zero[e] = 0.0f;
-    uint32_t *mask = sm;                         // [E][kWords]
-    uint32_t *pre = mask + (size_t)E * kWords;   // [E][kWords]
-    int *tot = reinterpret_cast<int *>(pre + (size_t)E * kWords);  // [E]
+    const int P = mask_pitch(E);
+    uint32_t *mask = sm;                         // [kWords][P]
+    uint32_t *pre = mask + (size_t)kWords * P;   // [kWords][P]
+    int *tot = reinterpret_cast<int *>(pre + (size_t)kWords * P);  // [E]
     int *base = tot + E;                         // [E]
     int *off = base + E;                         // [E]
     int *myhist = off + E;                       // [E] this CTA's totals (cluster variant)
@@ -164,7 +173,7 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
 #pragma unroll
     for (int j = 0; j < kRegSlots; ++j)
         raw[j] = (t < T && j < k) ? topk[t * k + j] : -1;
-    for (int i = tid; i < E * kWords; i += kChunk)
+    for (int i = tid; i < kWords * P; i += kChunk)
         mask[i] = 0u;
     __syncthreads();
 
@@ -188,15 +197,14 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
             }
         }
         ev[j] = e;
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0u)
-            mask[e * kWords + warp] |= peers;
+        if (e >= 0)
+            atomicOr(&mask[warp * P + e], 1u << lane);
     }
     if (bad)
         raise_status(status, bad);
     __syncthreads();
     for (int e = warp; e < E; e += kChunk / 32) {
-        const uint32_t c = (lane < kWords) ? __popc(mask[e * kWords + lane]) : 0u;
+        const uint32_t c = (lane < kWords) ? __popc(mask[lane * P + e]) : 0u;
         uint32_t x = c;
 #pragma unroll
         for (int o = 1; o < kWords; o <<= 1) {
@@ -205,7 +213,7 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
                 x += y;
         }
         if (lane < kWords)
-            pre[e * kWords + lane] = x - c;
+            pre[lane * P + e] = x - c;
         if (lane == kWords - 1) {
             if (kCluster)
                 myhist[e] = (int)x;
@@ -217,14 +225,14 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
 #pragma unroll
     for (int j = 0; j < kRegSlots; ++j) {
         const int e = ev[j];
-        rk[j] = e >= 0 ? (int)(pre[e * kWords + warp] + __popc(mask[e * kWords + warp] & ((1u << lane) - 1u))) : 0;
+        rk[j] = e >= 0 ? (int)(pre[warp * P + e] + __popc(mask[warp * P + e] & ((1u << lane) - 1u))) : 0;
     }
 
     if (kCluster) {
         cluster_sync();   // every CTA's totals written
         for (int e = tid; e < E; e += kChunk) {
             int p = 0, all = 0;
-#pragma unroll 8
+#pragma unroll 16
             for (int c = 0; c < nctas; ++c) {
                 const int h = (int)ld_dsmem_u32(myhist + e, (uint32_t)c);
                 p += (c < cta) ? h : 0;
@@ -243,7 +251,8 @@ route_plan_reg_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int
         }
         for (int e = tid; e < E; e += kChunk) {
             int p = 0, all = 0;
-#pragma unroll 8
+            // 32 totals in flight per thread
+#pragma unroll 32
             for (int c = 0; c < nctas; ++c) {
                 const int h = __ldcg(hist + (int64_t)c * E + e);
                 p += (c < cta) ? h : 0;
@@ -284,9 +293,10 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
     if (amax_zero && blockIdx.x == 0)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             amax_zero[e] = 0.0f;
-    uint32_t *mask = sm;                         // [E][kWords]
-    uint32_t *pre = mask + (size_t)E * kWords;   // [E][kWords]
-    int *run = reinterpret_cast<int *>(pre + (size_t)E * kWords);  // [E]
+    const int P = mask_pitch(E);
+    uint32_t *mask = sm;                         // [kWords][P]
+    uint32_t *pre = mask + (size_t)kWords * P;   // [kWords][P]
+    int *run = reinterpret_cast<int *>(pre + (size_t)kWords * P);  // [E]
     int *base = run + E;                         // [E]
     int *off = base + E;                         // [E]
     __shared__ int wtmp[32];
@@ -304,7 +314,7 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
     uint32_t bad = 0;
     for (int ch = 0; ch < chunks_per_cta; ++ch) {
         const int64_t t = ((int64_t)cta * chunks_per_cta + ch) * kChunk + tid;
-        for (int i = tid; i < E * kWords; i += kChunk)
+        for (int i = tid; i < kWords * P; i += kChunk)
             mask[i] = 0u;
         __syncthreads();
         for (int j = 0; j < k; ++j) {
@@ -326,16 +336,14 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
                 }
                 dest[t * k + j] = e; // validated expert id, consumed below
             }
-            // lanes routed to the same expert in this slot own their bits of
-            // word `warp` of that expert's mask; the lowest such lane writes them
-            const uint32_t peers = __match_any_sync(0xffffffffu, e);
-            if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0u)
-                mask[e * kWords + warp] |= peers;
+            // each lane owns its bit of word `warp` of its expert's mask
+            if (e >= 0)
+                atomicOr(&mask[warp * P + e], 1u << lane);
         }
         __syncthreads();
         // exclusive prefix over the chunk's words of every expert (+ the run)
         for (int e = warp; e < E; e += kChunk / 32) {
-            const uint32_t c = (lane < kWords) ? __popc(mask[e * kWords + lane]) : 0u;
+            const uint32_t c = (lane < kWords) ? __popc(mask[lane * P + e]) : 0u;
             uint32_t x = c;
 #pragma unroll
             for (int o = 1; o < kWords; o <<= 1) {
@@ -345,7 +353,7 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
             }
             const int r0 = run[e];
             if (lane < kWords)
-                pre[e * kWords + lane] = (uint32_t)r0 + x - c;
+                pre[lane * P + e] = (uint32_t)r0 + x - c;
             __syncwarp();
             if (lane == kWords - 1)
                 run[e] = r0 + (int)x;
@@ -355,8 +363,8 @@ route_plan_kernel(const int32_t *__restrict__ topk, int T, int k, int E, int A, 
             for (int j = 0; j < k; ++j) {
                 const int e = dest[t * k + j];
                 if (e >= 0) {
-                    const uint32_t below = mask[e * kWords + warp] & ((1u << lane) - 1u);
-                    const int rank = (int)(pre[e * kWords + warp] + __popc(below));
+                    const uint32_t below = mask[warp * P + e] & ((1u << lane) - 1u);
+                    const int rank = (int)(pre[warp * P + e] + __popc(below));
                     dest[t * k + j] = (e << kRankBits) | rank;
                 }
             }
@@ -423,26 +431,32 @@ cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, in
                               int32_t *offsets, int32_t *counts, int32_t *dest, int32_t *hist,
                               uint32_t *status, float *amax_zero)
 {
-    const size_t smem = (size_t)E * kWords * 4u * 2u + (size_t)E * 4u * 4u;
+    const size_t smem = (size_t)mask_pitch(E) * kWords * 4u * 2u + (size_t)E * 4u * 4u;
     static std::atomic<uint32_t> done[2] = {}, done_reg[2] = {}, done_cl[2] = {};
-    cudaError_t err = ensure_smem_limit(route_plan_kernel, c.device, 1024 * kWords * 8 + 1024 * 16, done);
+    cudaError_t err = ensure_smem_limit(route_plan_kernel, c.device, 1025 * kWords * 8 + 1024 * 16, done);
     if (err == cudaSuccess)
-        err = ensure_smem_limit(route_plan_reg_kernel<false>, c.device, 1024 * kWords * 8 + 1024 * 16, done_reg);
+        err = ensure_smem_limit(route_plan_reg_kernel<false>, c.device, 1025 * kWords * 8 + 1024 * 16, done_reg);
     if (err == cudaSuccess)
-        err = ensure_smem_limit(route_plan_reg_kernel<true>, c.device, 1024 * kWords * 8 + 1024 * 16, done_cl);
+        err = ensure_smem_limit(route_plan_reg_kernel<true>, c.device, 1025 * kWords * 8 + 1024 * 16, done_cl);
     if (err != cudaSuccess)
         return err;
-    int per_sm = 0;
+    // each cooperative form is sized by its own kernel's residency
+    int per_sm = 0, per_sm_reg = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_plan_kernel, kChunk, smem);
+    if (err == cudaSuccess)
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_reg, route_plan_reg_kernel<false>, kChunk, smem);
     if (err != cudaSuccess)
         return err;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
     const int nch = (T + kChunk - 1) / kChunk;
+    // one chunk per CTA with the slots in registers when k <= 8 and every
+    // chunk's CTA can be resident; else runs of chunks per CTA
+    const bool reg = k <= kRegSlots && nch <= per_sm_reg * c.num_sms;
     const int max_ctas = per_sm * c.num_sms;
     int nctas = nch < 1 ? 1 : nch;
     int cpc = 1;
-    if (nctas > max_ctas) {
+    if (!reg && nctas > max_ctas) {
         cpc = (nch + max_ctas - 1) / max_ctas;
         nctas = (nch + cpc - 1) / cpc;
     }
@@ -456,7 +470,7 @@ cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, in
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cpc == 1 && k <= kRegSlots && nctas <= kMaxClusterCtas) {
+    if (reg && nctas <= kMaxClusterCtas) {
         // one cluster of all CTAs, if the device can place it
         // (placement answer cached per device, cluster size and shared-memory size class)
         static std::mutex mu;
@@ -493,7 +507,7 @@ cudaError_t launch_route_plan(const LaunchCtx &c, const int32_t *topk, int T, in
             return cudaLaunchKernelEx(&ccfg, route_plan_reg_kernel<true>, topk, T, k, E, A, offsets, counts, dest,
                                       reinterpret_cast<uint32_t *>(hist), status, amax_zero);
     }
-    if (cpc == 1 && k <= kRegSlots)
+    if (reg)
         return cudaLaunchKernelEx(&cfg, route_plan_reg_kernel<false>, topk, T, k, E, A, offsets, counts, dest,
                                   reinterpret_cast<uint32_t *>(hist), status, amax_zero);
     return cudaLaunchKernelEx(&cfg, route_plan_kernel, topk, T, k, E, A, cpc, offsets, counts, dest,

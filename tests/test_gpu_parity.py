@@ -296,10 +296,12 @@ def test_pointer_off_the_input_device_is_refused():
     assert s == 0 and int(off[E].item()) == 2 * 128
 
 
-@pytest.mark.parametrize("T,E,k", [(3000, 32, 12), (400000, 64, 2), (20000, 1024, 3)])
+@pytest.mark.parametrize("T,E,k", [(3000, 32, 12), (400000, 64, 2), (20000, 1024, 3), (200000, 64, 4)])
 def test_route_plan_general_paths(T, E, k):
-    """Routing alone on shapes that leave the register fast path: k > 8, and
-    more 512-token chunks than resident CTAs (several chunks per CTA)."""
+    """Routing alone on shapes that leave the register fast path: k > 8, more
+    512-token chunks than resident CTAs (several chunks per CTA), and more
+    chunks than the register kernel can keep resident but not than the
+    general kernel can (one chunk per CTA on the general kernel)."""
     rng = np.random.default_rng(T + k)
     topk = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
     topk[rng.random((T, k)) < 0.02] = -1
