@@ -284,10 +284,15 @@ class BufferSet:
         torch.cuda.synchronize()
 
 
-STEP_STREAMS = 2
+def step_streams(set_bytes: int) -> int:
+    """Streams that take alternate steps: three for batches whose buffer set
+    holds less than 1 GB (their steps are short against the kernels' start-up
+    and tail), two for larger ones (a third stream measured no faster on the
+    16384-token, 256-expert batch and slower on the 64-expert one)."""
+    return 3 if set_bytes < (1 << 30) else 2
 
 
-def capture_rotation(torch, sets, rotations: int = 1, streams: int = STEP_STREAMS):
+def capture_rotation(torch, sets, rotations: int = 1, streams: int = 2):
     """One graph holding `rotations` rounds of one step on every buffer set,
     in rotation order, the steps dealt in turn to `streams` streams (the
     batches are independent: one stream's step runs while the other's starts
@@ -332,7 +337,8 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
     R_cap = nq.rows_capacity(T, k, E, w.A)
     set_bytes = 2 * T * H + 4 * T * k + R_cap * S * 2 + R_cap * (9 * H // 8 + 4)
     nset = n_rotating_sets(set_bytes, n_sets)
-    nset += (-nset) % STEP_STREAMS   # every stream keeps its own sets
+    ns = step_streams(set_bytes)
+    nset += (-nset) % ns   # every stream keeps its own sets
     sets = [BufferSet(torch, nq, w, tok_host, topk_host) for _ in range(nset)]
     torch.cuda.synchronize()
     st = int(sets[0].plan.status.item())
@@ -343,11 +349,11 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
         b.capture(torch)
     GRAPH_ROTATIONS = 50
     SAMPLE_EVERY = 10
-    gR = capture_rotation(torch, sets)
+    gR = capture_rotation(torch, sets, 1, ns)
     nblocks, rem = divmod(K, nset)
     n_big, n_small = divmod(nblocks, GRAPH_ROTATIONS)
-    gBig = capture_rotation(torch, sets, GRAPH_ROTATIONS) if n_big else None
-    gSmall = capture_rotation(torch, sets, n_small) if n_small else None
+    gBig = capture_rotation(torch, sets, GRAPH_ROTATIONS, ns) if n_big else None
+    gSmall = capture_rotation(torch, sets, n_small, ns) if n_small else None
     clocks = ClockSampler(gpu_index, enabled=clocks_enabled)
     clocks.start()
     time.sleep(0.1)
@@ -398,7 +404,8 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
     st = int(sets[0].plan.status.item())
     route_b, pack_b, dr_b = algorithmic_bytes(T, H, k, E, R, S)
     set_mb = (route_b + pack_b + dr_b) / 1e6
-    return dict(sets=sets, tok_host=tok_host, topk_host=topk_host, nset=nset, set_mb=set_mb, T=T, H=H, k=k, E=E,
+    return dict(sets=sets, tok_host=tok_host, topk_host=topk_host, nset=nset, streams=ns, set_mb=set_mb, T=T, H=H,
+                k=k, E=E,
                 R=R, S=S, ms_total=ms_total, ms_step=ms_total / K, ms_a=ms_a, ms_b=ms_b, wall_s=wall1 - wall0,
                 clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), w=w, n_sampled_steps=len(flat), K=K, W=W)
 
@@ -416,7 +423,7 @@ def step_report(r, peak, peak_kind, world=1, config=None, n_sets_note=True) -> d
            "rounding": "sr" if w.rounding else "rne",
            "l2": f"{r['nset']} rotating buffer sets ({r['set_mb']:.0f} MB touched per step; a set is reused "
                  f"after the others moved {(r['nset'] - 1) * r['set_mb']:.0f} MB through the 129 MB L2), "
-                 f"CUDA-graph steps, {STEP_STREAMS} streams taking alternate steps",
+                 f"CUDA-graph steps, {r.get('streams', 1)} streams taking alternate steps",
            "parallelism": f"replicas x{world}"}
     return {
         "value": tokens_s, "unit": UNIT, "ms_per_step": r["ms_step"], "steps": r["K"], "warmup": r["W"],
