@@ -66,7 +66,8 @@ def parse_args():
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-extra-configs", action="store_true",
                    help="only the headline workload (no nested configs 2, 3 and the config-5 comparison)")
-    p.add_argument("--sets", type=int, default=0, help="rotating buffer sets (0: enough to exceed the L2)")
+    p.add_argument("--sets", type=int, default=0, help="rotating buffer sets (0: enough to exceed the L2); rounded up to "
+                   "a multiple of the streams that take alternate steps")
     p.add_argument("--config", type=int, default=WORKLOAD_CFG, choices=[1, 2, 3, 4, 5],
                    help="headline workload (default: the largest, the 16384x7168 SR combine-backward batch)")
     p.add_argument("--tokens", type=int, default=0,
