@@ -69,3 +69,20 @@ def test_traffic_comes_only_from_a_record_of_the_current_sources(tmp_path):
     other.write_text("// not the receive\n")
     assert bench.profiled_traffic("direct_receive", [os.path.relpath(other, ROOT)], 4) is None
     assert bench.profiled_traffic("direct_receive", bench.DR_SOURCES, 3) is None
+
+
+def test_step_streams_and_set_rounding():
+    """Small batches take three streams, large ones two, and the rotating
+    sets are a multiple of the stream count, so a set stays on one stream."""
+    assert bench.step_streams(128 << 20) == 3 and bench.step_streams(900 << 20) == 3
+    assert bench.step_streams(1 << 30) == 2 and bench.step_streams(3 << 30) == 2
+    for set_bytes in (64 << 20, 128 << 20, 700 << 20, 2 << 30, 3 << 30):
+        ns = bench.step_streams(set_bytes)
+        n = bench.n_rotating_sets(set_bytes)
+        n += (-n) % ns
+        assert n % ns == 0 and n >= 2
+        # step j runs on stream j mod ns; set j mod n: one stream per set
+        owners = {}
+        for j in range(5 * n):
+            owners.setdefault(j % n, set()).add(j % ns)
+        assert all(len(v) == 1 for v in owners.values())
