@@ -272,12 +272,8 @@ class BufferSet:
     def capture(self, torch):
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
-        self.gA, self.gB, self.gS = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        self.gS = torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
-            with torch.cuda.graph(self.gA, stream=s):
-                self.route_pack()
-            with torch.cuda.graph(self.gB, stream=s):
-                self.receive()
             with torch.cuda.graph(self.gS, stream=s):
                 self.route_pack()
                 self.receive()
@@ -327,10 +323,11 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
     single steps for a remainder), so the device runs the steps back to back
     with a launch gap only between graphs; inside a graph two streams take
     alternate steps (independent batches), so one step's start-up and tail
-    overlap the other stream's step.  After the timed region one
-    rotation in ten is replayed call by call with CUDA events between the
-    calls, which gives the per-call durations of the roofline (those steps
-    stop the calls' overlap and are not part of the step time)."""
+    overlap the other stream's step.  After the timed region each call kind
+    (route plan + pack; direct receive) runs alone, back to back over the
+    rotating sets in a graph of its own on one stream: its device time over
+    the calls is the per-call duration of the roofline (not part of the step
+    time)."""
     T, H, k, E = w.T, w.H, w.k, w.E
     tok_host = torch.from_numpy(w.tokens.view(np.int16)).view(torch.bfloat16)
     topk_host = torch.from_numpy(np.ascontiguousarray(w.topk))
@@ -349,7 +346,7 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
     for b in sets:
         b.capture(torch)
     GRAPH_ROTATIONS = 50
-    SAMPLE_EVERY = 10
+    CALLS_TIMED = 20     # calls of each kind behind the per-call durations
     gR = capture_rotation(torch, sets, 1, ns)
     nblocks, rem = divmod(K, nset)
     n_big, n_small = divmod(nblocks, GRAPH_ROTATIONS)
@@ -387,28 +384,45 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
     clocks.stop()
     clk = clocks.summary(wall0, wall1, busy0)
     ms_total = t0.elapsed_time(t1)
-    n_sampled = max(1, (nblocks + SAMPLE_EVERY - 1) // SAMPLE_EVERY)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(nset)] for _ in range(n_sampled)]
-    for blk in range(n_sampled):
-        for j, b in enumerate(sets):
-            e = ev[blk][j]
-            e[0].record()
-            b.gA.replay()
-            e[1].record()
-            b.gB.replay()
-            e[2].record()
-    torch.cuda.synchronize()
-    flat = [e for row in ev for e in row]
-    ms_a = float(np.mean([e[0].elapsed_time(e[1]) for e in flat]))
-    ms_b = float(np.mean([e[1].elapsed_time(e[2]) for e in flat]))
+    # per-call durations (the roofline's): each call alone, back to back over
+    # the rotating sets in one graph on one stream, device time / calls
+    def calls_graph(call, rotations):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(rotations):
+                    for b in sets:
+                        getattr(b, call)()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return g
+
+    call_rot = max(1, math.ceil(CALLS_TIMED / nset))
+    per_call = []
+    for call in ("route_pack", "receive"):
+        g = calls_graph(call, call_rot)
+        g.replay()   # the first launch also uploads the graph
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b_.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b_) / (call_rot * nset))
+        per_call.append(float(np.median(ts)))
+        del g
+    ms_a, ms_b = per_call
     st = int(sets[0].plan.status.item())
     route_b, pack_b, dr_b = algorithmic_bytes(T, H, k, E, R, S)
     set_mb = (route_b + pack_b + dr_b) / 1e6
     return dict(sets=sets, tok_host=tok_host, topk_host=topk_host, nset=nset, streams=ns, set_mb=set_mb, T=T, H=H,
                 k=k, E=E,
                 R=R, S=S, ms_total=ms_total, ms_step=ms_total / K, ms_a=ms_a, ms_b=ms_b, wall_s=wall1 - wall0,
-                clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), w=w, n_sampled_steps=len(flat), K=K, W=W)
+                clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), w=w, n_calls_timed=call_rot * nset, K=K, W=W)
 
 
 def step_report(r, peak, peak_kind, world=1, config=None, n_sets_note=True) -> dict:
@@ -438,7 +452,7 @@ def step_report(r, peak, peak_kind, world=1, config=None, n_sets_note=True) -> d
                      "traffic": profiled_traffic("direct_receive", DR_SOURCES, config)},
         "clocks": r["clocks"],
         "device_status": r["status"],
-        "sampled_steps_for_kernel_times": r["n_sampled_steps"],
+        "calls_for_kernel_times": r["n_calls_timed"],
     }
 
 
@@ -929,7 +943,7 @@ def main():
                                "note": "one call on the step's batch, L2 flushed before each launch"}
                         for name, v in r["aux"].items()},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
-        "sampled_steps_for_kernel_times": r["n_sampled_steps"],
+        "calls_for_kernel_times": r["n_calls_timed"],
         "clocks": r["clocks"],
         "device_status": r["status"],
         "timed_wall_s": r["wall_s"],

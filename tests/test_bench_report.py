@@ -19,7 +19,7 @@ def record(T=16384, H=7168, k=8, E=256, R=147200, ms_step=0.75, ms_a=0.15, ms_b=
     S = (9 * H // 16 + 16 + 15) // 16 * 16
     w = types.SimpleNamespace(description="synthetic", A=128, rounding=1)
     return dict(w=w, T=T, H=H, k=k, E=E, R=R, S=S, nset=2, set_mb=2600.0, ms_step=ms_step, ms_a=ms_a, ms_b=ms_b,
-                K=100, W=10, clocks=None, status=0, n_sampled_steps=20,
+                K=100, W=10, clocks=None, status=0, n_calls_timed=20,
                 bytes=bench.algorithmic_bytes(T, H, k, E, R, S))
 
 
