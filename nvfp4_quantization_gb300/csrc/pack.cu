@@ -591,6 +591,64 @@ nvfp4_pack_warp_kernel(const uint16_t *__restrict__ tokens, int T, int H, const 
         pdl_launch_dependents();
 }
 
+// One MXFP8 block of 32 values (16 words of BF16 pairs) -> its 32 E4M3 bytes
+// (o, in element order) and its E8M0 scale byte: e = the smallest integer in
+// [-127, 127] with max|x| <= 448 * 2^e, elements E4M3_RNE(x / 2^e).
+__device__ __forceinline__ void mxfp8_encode32(const uint32_t (&w)[16], uint32_t (&o)[8], uint32_t &sbyte)
+{
+    const uint32_t b = max(absmax16_bits(&w[0]), absmax16_bits(&w[8]));
+    // smallest e in [-127, 127] with B <= 448 * 2^e; 448 = 1.75 * 2^8, i.e.
+    // BF16 exponent field 135 with mantissa field 96
+    const int ef = (b >> 7) & 0xff, mt = b & 0x7f;
+    int e = (ef == 0) ? -127 : ef - 135 + (mt > 96 ? 1 : 0);
+    e = max(-127, min(127, e));
+    const float f = (e <= 126) ? exp2i(-e) : u2f(0x00400000u); // 2^-e
+    const float2 f2 = make_float2(f, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 a = mul2(make_float2(bf16lo(w[2 * i]), bf16hi(w[2 * i])), f2);
+        const float2 bb = mul2(make_float2(bf16lo(w[2 * i + 1]), bf16hi(w[2 * i + 1])), f2);
+        o[i] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(bb.x, bb.y) << 16);
+    }
+    sbyte = (uint32_t)(e + 127);
+}
+
+// Block q's 32 bytes and scale byte to every destination row of its token.
+// The scale bytes of four neighbouring blocks (lanes 4i .. 4i + 3 of a warp)
+// leave as one word when a row's scales are a whole number of words; the four
+// lanes of a group are then all present (the block size is a multiple of 32
+// and q < nq holds for all four or none), and only they take part in the
+// exchange.
+__device__ __forceinline__ void mxfp8_store_block(const uint32_t (&o)[8], uint32_t sbyte, int q, int nq, int H,
+                                                  const int *sdest, int k, uint8_t *buf, uint8_t *scales, int R_cap,
+                                                  uint32_t *status)
+{
+    const bool wordwise = (nq & 3) == 0;
+    uint32_t sw = sbyte << (8 * (q & 3));
+    if (wordwise) {
+        const uint32_t grp = 0xfu << (threadIdx.x & 28u);
+        sw |= __shfl_xor_sync(grp, sw, 1);
+        sw |= __shfl_xor_sync(grp, sw, 2);
+    }
+    for (int j = 0; j < k; ++j) {
+        const int d = sdest[j];
+        if (d < 0)
+            continue;
+        if (d >= R_cap) {
+            raise_status(status, kDevErrCapacity);
+            continue;
+        }
+        uint8_t *row = buf + (int64_t)d * H + (int64_t)q * 32;
+        st16(row, make_uint4(o[0], o[1], o[2], o[3]));
+        st16(row + 16, make_uint4(o[4], o[5], o[6], o[7]));
+        if (!wordwise)
+            scales[(int64_t)d * (H / 32) + q] = (uint8_t)sbyte;
+        else if ((q & 3) == 0)
+            *reinterpret_cast<uint32_t *>(scales + (int64_t)d * (H / 32) + q) = sw;
+    }
+}
+
+// MXFP8 pack, one CTA per token (H / 32 > kMaxThreads: several blocks per thread).
 __global__ void __launch_bounds__(kMaxThreads)
 mxfp8_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32_t *__restrict__ dest,
                   int k, const int32_t *__restrict__ offsets, const int32_t *__restrict__ counts, int E,
@@ -621,50 +679,68 @@ mxfp8_pack_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32
             const uint4 v = ld_stream16(src + (int64_t)q * 64 + p * 16);
             w[4 * p + 0] = v.x; w[4 * p + 1] = v.y; w[4 * p + 2] = v.z; w[4 * p + 3] = v.w;
         }
-        const uint32_t b = max(absmax16_bits(&w[0]), absmax16_bits(&w[8]));
-        // smallest e in [-127, 127] with B <= 448 * 2^e; 448 = 1.75 * 2^8, i.e.
-        // BF16 exponent field 135 with mantissa field 96
-        const int ef = (b >> 7) & 0xff, mt = b & 0x7f;
-        int e = (ef == 0) ? -127 : ef - 135 + (mt > 96 ? 1 : 0);
-        e = max(-127, min(127, e));
-        const float f = (e <= 126) ? exp2i(-e) : u2f(0x00400000u); // 2^-e
-        const float2 f2 = make_float2(f, f);
-        uint32_t o[8];
+        uint32_t o[8], sbyte;
+        mxfp8_encode32(w, o, sbyte);
+        mxfp8_store_block(o, sbyte, q, nq, H, sdest, k, buf, scales, R_cap, status);
+    }
+}
+
+// MXFP8 pack, persistent (H / 32 <= the block size: one block per thread):
+// the resident token CTAs walk the tokens, each issuing the next token's loads
+// (and reading its destinations) before it encodes and stores the current one;
+// CTAs past the token CTAs write the padding rows.
+__global__ void __launch_bounds__(kMaxThreads)
+mxfp8_pack_persistent_kernel(const uint16_t *__restrict__ tokens, int T, int H, const int32_t *__restrict__ dest,
+                             int k, const int32_t *__restrict__ offsets, const int32_t *__restrict__ counts, int E,
+                             uint8_t *__restrict__ buf, int R_cap, uint32_t *__restrict__ status, int pad_ctas,
+                             int n_tok_ctas)
+{
+    __shared__ int sdest[2][32];
+    pdl_launch_dependents();
+    pdl_wait();
+    if ((int)blockIdx.x >= n_tok_ctas) {
+        fill_padding(1, blockIdx.x - n_tok_ctas, pad_ctas, offsets, counts, E, R_cap, buf, 0, H, status);
+        return;
+    }
+    const int nq = H / 32;
+    const int q = threadIdx.x;
+    const bool mine = q < nq;
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(tokens);
+    uint8_t *scales = buf + (int64_t)R_cap * H;
+    auto load = [&](int t, uint32_t(&w)[16]) {
+        const uint8_t *src = base + (int64_t)t * H * 2 + (int64_t)q * 64;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float2 a = mul2(make_float2(bf16lo(w[2 * i]), bf16hi(w[2 * i])), f2);
-            const float2 bb = mul2(make_float2(bf16lo(w[2 * i + 1]), bf16hi(w[2 * i + 1])), f2);
-            o[i] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(bb.x, bb.y) << 16);
+        for (int p = 0; p < 4; ++p) {
+            const uint4 v = ld_stream16(src + p * 16);
+            w[4 * p + 0] = v.x; w[4 * p + 1] = v.y; w[4 * p + 2] = v.z; w[4 * p + 3] = v.w;
         }
-        const uint32_t sbyte = (uint32_t)(e + 127);
-        // the scale bytes of four neighbouring blocks (lanes 4i .. 4i + 3 of
-        // a warp) leave as one word when a row's scales are a whole number of
-        // words; the four lanes of a group are then all present (the block
-        // size is a multiple of 32 and q < nq holds for all four or none),
-        // and only they take part in the exchange
-        const bool wordwise = (nq & 3) == 0;
-        uint32_t sw = sbyte << (8 * (q & 3));
-        if (wordwise) {
-            const uint32_t grp = 0xfu << (threadIdx.x & 28u);
-            sw |= __shfl_xor_sync(grp, sw, 1);
-            sw |= __shfl_xor_sync(grp, sw, 2);
+    };
+    int t = blockIdx.x;
+    uint32_t w[16];
+    if (t < T) {
+        if (mine)
+            load(t, w);
+        if (threadIdx.x < k)
+            sdest[0][threadIdx.x] = dest[(int64_t)t * k + threadIdx.x];
+    }
+    for (int i = 0; t < T; t += n_tok_ctas, ++i) {
+        __syncthreads();   // this token's destinations are in sdest[i & 1]
+        const int tn = t + n_tok_ctas;
+        uint32_t wn[16];
+        if (tn < T) {
+            if (mine)
+                load(tn, wn);
+            if (threadIdx.x < k)
+                sdest[(i + 1) & 1][threadIdx.x] = dest[(int64_t)tn * k + threadIdx.x];
         }
-        for (int j = 0; j < k; ++j) {
-            const int d = sdest[j];
-            if (d < 0)
-                continue;
-            if (d >= R_cap) {
-                raise_status(status, kDevErrCapacity);
-                continue;
-            }
-            uint8_t *row = buf + (int64_t)d * H + (int64_t)q * 32;
-            st16(row, make_uint4(o[0], o[1], o[2], o[3]));
-            st16(row + 16, make_uint4(o[4], o[5], o[6], o[7]));
-            if (!wordwise)
-                scales[(int64_t)d * (H / 32) + q] = (uint8_t)sbyte;
-            else if ((q & 3) == 0)
-                *reinterpret_cast<uint32_t *>(scales + (int64_t)d * (H / 32) + q) = sw;
+        if (mine) {
+            uint32_t o[8], sbyte;
+            mxfp8_encode32(w, o, sbyte);
+            mxfp8_store_block(o, sbyte, q, nq, H, sdest[i & 1], k, buf, scales, R_cap, status);
         }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            w[j] = wn[j];
     }
 }
 
@@ -792,6 +868,20 @@ cudaError_t launch_mxfp8_pack(const LaunchCtx &c, const uint16_t *tokens, int T,
     const int cpt = (nq + kMaxThreads - 1) / kMaxThreads;
     const int th = pack_threads(H, cpt);
     const int pc = padding_ctas(c, E);
+    if (cpt == 1) {
+        // one wave of resident CTAs walks all tokens
+        int per_sm = 0;
+        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_pack_persistent_kernel, th, 0);
+        if (err != cudaSuccess)
+            return err;
+        int64_t tc = (int64_t)c.num_sms * (per_sm < 1 ? 1 : per_sm);
+        if (tc > T)
+            tc = T;
+        if (tc < 1)
+            tc = 1;
+        return launch_pdl(mxfp8_pack_persistent_kernel, dim3((unsigned)(tc + pc)), dim3(th), 0, c.stream, tokens, T,
+                          H, dest, k, offsets, counts, E, buf, R_cap, status, pc, (int)tc);
+    }
     return launch_pdl(mxfp8_pack_kernel, dim3(T + pc), dim3(th), 0, c.stream, tokens, T, H,
                       dest, k, offsets, counts, E, buf, R_cap, status, pc, cpt);
 }
