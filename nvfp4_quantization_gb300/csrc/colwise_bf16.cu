@@ -25,7 +25,6 @@
 
 namespace epq {
 
-constexpr int kCbThreads = 256;      // MXFP8 columnwise
 constexpr int kCbMaxExperts = 1024;
 
 constexpr int kCbWarps = 12;         // RHT operand: warps of a CTA, one CTA per SM
@@ -286,20 +285,42 @@ colwise_rht_bf16_kernel(const __grid_constant__ CUtensorMap tm_x, int H, int R_c
 // the expert-output gradient as a per-expert MXFP8 GroupedTensor): blocks of
 // 32 consecutive rows of one expert per hidden column, the E8M0 exponent e the
 // smallest in [-127, 127] with max|x| <= 448 * 2^e, elements E4M3_RNE(x / 2^e).
-// Work unit of a warp: 128 rows x 64 columns of one expert; lane l takes the
-// column pair l and the four 32-row blocks in turn: 32 loads of 4 bytes (a
-// warp's load is one 128-byte row segment), the two columns' block maxima on
-// the BF16 bit patterns, 32 data bytes per column (one sector) per block and,
-// after the four blocks, the column's 4 scale bytes in one store.
-__global__ void __launch_bounds__(kCbThreads)
-mxfp8_colwise_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const int32_t *__restrict__ offsets, int E,
-                     uint8_t *__restrict__ buf, uint32_t *__restrict__ status)
+// Work unit of a warp: 128 rows x 64 columns of one expert (16 KB of BF16),
+// streamed through the warp's own two-stage TMA ring; lane l takes the column
+// pair l and the unit's four 32-row blocks in turn, reading each block's 32
+// words from the stage: the two columns' block maxima on the BF16 bit
+// patterns, 32 data bytes per column (one sector) per block, so each column's
+// 128-byte line of the unit comes from one lane, and after the four blocks the
+// column's 4 scale bytes in one store.
+constexpr int kMxWarps = 6;          // warps of a CTA, one CTA per SM
+constexpr int kMxUnitRows = 128;
+constexpr uint32_t kMxUnitBytes = kMxUnitRows * kCbUnitWords * 4;
+
+struct __align__(128) MxSmem {
+    uint32_t stage[kMxWarps][kCbStages][kMxUnitRows * kCbUnitWords];
+    uint64_t full[kMxWarps][kCbStages];
+    // followed by the expert offsets [E + 1] (int)
+};
+
+template <bool kV8>
+__global__ void __launch_bounds__(kMxWarps * 32, 1)
+mxfp8_colwise_kernel(const __grid_constant__ CUtensorMap tm_x, int H, int R_cap, const int32_t *__restrict__ offsets,
+                     int E, uint8_t *__restrict__ buf, uint32_t *__restrict__ status)
 {
-    __shared__ int offs[kCbMaxExperts + 1];
+    extern __shared__ uint8_t mx_smem_raw[];
+    MxSmem &sm = *reinterpret_cast<MxSmem *>((reinterpret_cast<uintptr_t>(mx_smem_raw) + 127) & ~(uintptr_t)127);
+    int *offs = reinterpret_cast<int *>(&sm + 1);   // [E + 1]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (lane == 0) {
+        for (int s = 0; s < kCbStages; ++s)
+            mbar_init(&sm.full[warp][s], 1);
+        fence_mbar_init();
+        if (warp == 0)
+            tma_prefetch_desc(&tm_x);
+    }
     pdl_launch_dependents();
     pdl_wait();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i <= E; i += kCbThreads)
+    for (int i = tid; i <= E; i += blockDim.x)
         offs[i] = __ldg(offsets + i);
     __syncthreads();
     int R = offs[E];
@@ -311,87 +332,131 @@ mxfp8_colwise_kernel(const uint32_t *__restrict__ x, int H, int R_cap, const int
     uint8_t *data = buf;
     uint8_t *scales = buf + (int64_t)R_cap * H;
     const int ngrp = (H + 63) / 64;
-    const int64_t n_units = (int64_t)(R / 128) * ngrp;
-    for (int64_t wu = (int64_t)blockIdx.x * (kCbThreads / 32) + warp; wu < n_units;
-         wu += (int64_t)gridDim.x * (kCbThreads / 32)) {
+    const int64_t n_units = (int64_t)(R / kMxUnitRows) * ngrp;
+    const int64_t stride = (int64_t)gridDim.x * kMxWarps;
+    const int64_t u0 = (int64_t)blockIdx.x * kMxWarps + warp;
+    uint32_t *const stg = sm.stage[warp][0];
+    uint64_t *const full = sm.full[warp];
+    auto issue = [&](int64_t u, int s) {
+        const int rb = (int)(u / ngrp), cg = (int)(u % ngrp);
+        mbar_arrive_expect_tx(&full[s], kMxUnitBytes);
+        tma_load_2d(stg + s * (kMxUnitRows * kCbUnitWords), &tm_x, 128 * cg, kMxUnitRows * rb, &full[s]);
+    };
+    int issued = 0;
+    if (lane == 0) {
+        for (int s = 0; s < kCbStages; ++s) {
+            if (u0 + s * stride >= n_units)
+                break;
+            issue(u0 + s * stride, s);
+            ++issued;
+        }
+    }
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+
+    int it = 0;
+    for (int64_t wu = u0; wu < n_units; wu += stride, ++it) {
+        const int s = it % kCbStages;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(it / kCbStages) & 1u))) {
+            if (lane == 0)
+                raise_status(status, kDevErrTimeout);
+            break;
+        }
         const int rb = (int)(wu / ngrp), cg = (int)(wu % ngrp);
-        const int row0 = 128 * rb;
+        const int row0 = kMxUnitRows * rb;
         const int e = cb_expert_of_row(offs, E, row0);
         const int off = offs[e], n = offs[e + 1] - off, rl = row0 - off;
-        if ((off & 127) != 0 || (n & 127) != 0) {
-            if (lane == 0)
-                raise_status(status, kDevErrBadExpert);
-            continue;
-        }
-        const int P = 32 * cg + lane;   // columns 2P and 2P + 1
-        if (2 * P >= H)
-            continue;
-        const int h0 = 2 * P;
-        uint32_t sw0 = 0u, sw1 = 0u;
+        const bool bad = (off & 127) != 0 || (n & 127) != 0;
+        if (bad && lane == 0)
+            raise_status(status, kDevErrBadExpert);   // an expert slot that is not whole 128-row tiles: skipped
+        const int h0 = 64 * cg + 2 * lane;            // columns h0 and h0 + 1
+        if (!bad && h0 < H) {
+            const uint32_t *src = stg + s * (kMxUnitRows * kCbUnitWords) + lane;
+            uint8_t *dp = data + (int64_t)off * H + (int64_t)h0 * n + rl;
+            uint32_t sw0 = 0u, sw1 = 0u;
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
-            const int r0 = row0 + 32 * b;
-            uint32_t wv[32];
+            for (int b = 0; b < 4; ++b) {
+                uint32_t wv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                wv[i] = __ldcs(x + (int64_t)(r0 + i) * (H / 2) + P);
-            // block maxima of both columns on the bit patterns (finite BF16:
-            // for non-negative values integer order is value order)
-            uint32_t m = wv[0];
+                for (int i = 0; i < 32; ++i)
+                    wv[i] = src[(32 * b + i) * kCbUnitWords];
+                // block maxima of both columns on the bit patterns (finite BF16:
+                // for non-negative values integer order is value order)
+                uint32_t m = wv[0];
 #pragma unroll
-            for (int i = 1; i < 32; ++i)
-                asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(wv[i]));
-            m &= 0x7fff7fffu;
-            float f[2];
-            uint32_t eb[2];
+                for (int i = 1; i < 32; ++i)
+                    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(wv[i]));
+                m &= 0x7fff7fffu;
+                float f[2];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint32_t bm = q ? (m >> 16) : (m & 0xffffu);
-                // smallest e in [-127, 127] with B <= 448 * 2^e; 448 = 1.75 * 2^8,
-                // i.e. BF16 exponent field 135 with mantissa field 96
-                const int ef = (int)((bm >> 7) & 0xffu), mt = (int)(bm & 0x7fu);
-                int ex = (ef == 0) ? -127 : ef - 135 + (mt > 96 ? 1 : 0);
-                ex = max(-127, min(127, ex));
-                f[q] = (ex <= 126) ? exp2i(-ex) : u2f(0x00400000u);   // 2^-e
-                eb[q] = (uint32_t)(ex + 127);
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t bm = q ? (m >> 16) : (m & 0xffffu);
+                    // smallest e in [-127, 127] with B <= 448 * 2^e; 448 = 1.75 * 2^8,
+                    // i.e. BF16 exponent field 135 with mantissa field 96
+                    const int ef = (int)((bm >> 7) & 0xffu), mt = (int)(bm & 0x7fu);
+                    int ex = (ef == 0) ? -127 : ef - 135 + (mt > 96 ? 1 : 0);
+                    ex = max(-127, min(127, ex));
+                    f[q] = (ex <= 126) ? exp2i(-ex) : u2f(0x00400000u);   // 2^-e
+                    if (q)
+                        sw1 |= (uint32_t)(ex + 127) << (8 * b);
+                    else
+                        sw0 |= (uint32_t)(ex + 127) << (8 * b);
+                }
+                uint32_t d0[8], d1[8];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float2 a0 = mul2(make_float2(bf16_lo(wv[i]), bf16_lo(wv[i + 1])), make_float2(f[0], f[0]));
+                    const float2 a1 = mul2(make_float2(bf16_lo(wv[i + 2]), bf16_lo(wv[i + 3])), make_float2(f[0], f[0]));
+                    const float2 c0 = mul2(make_float2(bf16_hi(wv[i]), bf16_hi(wv[i + 1])), make_float2(f[1], f[1]));
+                    const float2 c1 = mul2(make_float2(bf16_hi(wv[i + 2]), bf16_hi(wv[i + 3])), make_float2(f[1], f[1]));
+                    d0[i / 4] = cvt_e4m3x2(a0.x, a0.y) | (cvt_e4m3x2(a1.x, a1.y) << 16);
+                    d1[i / 4] = cvt_e4m3x2(c0.x, c0.y) | (cvt_e4m3x2(c1.x, c1.y) << 16);
+                }
+                st_global_32B(dp + 32 * b, make_uint2(d0[0], d0[1]), make_uint2(d0[2], d0[3]),
+                              make_uint2(d0[4], d0[5]), make_uint2(d0[6], d0[7]), kV8);
+                st_global_32B(dp + n + 32 * b, make_uint2(d1[0], d1[1]), make_uint2(d1[2], d1[3]),
+                              make_uint2(d1[4], d1[5]), make_uint2(d1[6], d1[7]), kV8);
             }
-            sw0 |= eb[0] << (8 * b);
-            sw1 |= eb[1] << (8 * b);
-            uint32_t d0[8], d1[8];
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                const float2 a0 = mul2(make_float2(bf16_lo(wv[i]), bf16_lo(wv[i + 1])), make_float2(f[0], f[0]));
-                const float2 a1 = mul2(make_float2(bf16_lo(wv[i + 2]), bf16_lo(wv[i + 3])), make_float2(f[0], f[0]));
-                const float2 c0 = mul2(make_float2(bf16_hi(wv[i]), bf16_hi(wv[i + 1])), make_float2(f[1], f[1]));
-                const float2 c1 = mul2(make_float2(bf16_hi(wv[i + 2]), bf16_hi(wv[i + 3])), make_float2(f[1], f[1]));
-                d0[i / 4] = cvt_e4m3x2(a0.x, a0.y) | (cvt_e4m3x2(a1.x, a1.y) << 16);
-                d1[i / 4] = cvt_e4m3x2(c0.x, c0.y) | (cvt_e4m3x2(c1.x, c1.y) << 16);
-            }
-            uint4 *dp = reinterpret_cast<uint4 *>(data + (int64_t)off * H + (int64_t)h0 * n + rl + 32 * b);
-            uint4 *dq = reinterpret_cast<uint4 *>(data + (int64_t)off * H + (int64_t)(h0 + 1) * n + rl + 32 * b);
-            dp[0] = make_uint4(d0[0], d0[1], d0[2], d0[3]);
-            dp[1] = make_uint4(d0[4], d0[5], d0[6], d0[7]);
-            dq[0] = make_uint4(d1[0], d1[1], d1[2], d1[3]);
-            dq[1] = make_uint4(d1[4], d1[5], d1[6], d1[7]);
+            uint8_t *sp = scales + (int64_t)off * (H / 32) + (int64_t)h0 * (n / 32) + rl / 32;
+            *reinterpret_cast<uint32_t *>(sp) = sw0;
+            *reinterpret_cast<uint32_t *>(sp + n / 32) = sw1;
         }
-        uint8_t *sp = scales + (int64_t)off * (H / 32) + (int64_t)h0 * (n / 32) + rl / 32;
-        *reinterpret_cast<uint32_t *>(sp) = sw0;
-        *reinterpret_cast<uint32_t *>(sp + n / 32) = sw1;
+        // every lane's reads of the stage are done: load it with the unit after next
+        __syncwarp();
+        if (wu + kCbStages * stride < n_units) {
+            if (lane == 0)
+                issue(wu + kCbStages * stride, s);
+            ++issued;
+        }
     }
+    // never leave with a load of this warp's ring in flight (after a wait that gave up)
+    if (lane == 0)
+        for (int i = it; i < issued; ++i)
+            (void)mbar_wait_bounded(&full[i % kCbStages], (uint32_t)(i / kCbStages) & 1u);
 }
 
 cudaError_t launch_mxfp8_colwise(const LaunchCtx &c, const uint16_t *x, int R_cap, int H, const int32_t *offsets,
                                  int E, uint8_t *buf, uint32_t *status)
 {
-    const int64_t units = (int64_t)(R_cap / 128) * ((H + 63) / 64);
-    int64_t grid = (units + (kCbThreads / 32) - 1) / (kCbThreads / 32);
-    const int64_t cap = (int64_t)c.num_sms * 4;
-    if (grid > cap)
-        grid = cap;
+    CUtensorMap tm_x;
+    if (!make_map(&tm_x, x, 2 * (uint64_t)H, (uint64_t)(R_cap > 0 ? R_cap : 1), 2 * (uint64_t)H,
+                  kCbUnitWords * 4, kMxUnitRows))
+        return cudaErrorInvalidValue;
+    const size_t smem = sizeof(MxSmem) + 128 + (size_t)(E + 1) * 4;
+    const bool v8 = (reinterpret_cast<uintptr_t>(buf) & 31u) == 0;
+    static std::atomic<uint32_t> done[2][2] = {};
+    auto kern = v8 ? mxfp8_colwise_kernel<true> : mxfp8_colwise_kernel<false>;
+    cudaError_t err = ensure_smem_limit(kern, c.device, (int)(sizeof(MxSmem) + 128 + (kCbMaxExperts + 1) * 4),
+                                        done[v8 ? 1 : 0]);
+    if (err != cudaSuccess)
+        return err;
+    const int64_t units = (int64_t)(R_cap / kMxUnitRows) * ((H + 63) / 64);
+    int64_t grid = (units + kMxWarps - 1) / kMxWarps;
+    if (grid > c.num_sms)
+        grid = c.num_sms;   // one resident CTA per SM
     if (grid < 1)
         grid = 1;
-    return launch_pdl(mxfp8_colwise_kernel, dim3((unsigned)grid), dim3(kCbThreads), 0, c.stream,
-                      reinterpret_cast<const uint32_t *>(x), H, R_cap, offsets, E, buf, status);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kMxWarps * 32), smem, c.stream, tm_x, H, R_cap, offsets, E,
+                      buf, status);
 }
 
 static CbRcp make_cb_rcp()
