@@ -135,6 +135,7 @@ struct DrArgs {
     // (moving them made the SR kernel spill)
     const float *amax_in;
     float *amax_row, *amax_col;
+    int grid_q, grid_r;   // the grid's CTA count divided by n_strips: quotient, remainder
 };
 
 // Tiles of a CTA: u = blockIdx.x + k * gridDim.x, k = 0, 1, ... over the tiles
@@ -170,6 +171,26 @@ __device__ __forceinline__ void issue_tile(Sm &sm, const CUtensorMap *tmc, const
     tma_load_2d(&sm.scales[s][0][0], tms, st * kScaleBytes, row0, &sm.full[s]);
     tma_load_2d(&sm.trailer[s][0][0], tmt, 0, row0, &sm.full[s]);
 }
+
+// The CTA's tiles u = blockIdx.x + it * gridDim.x in turn, as row tile
+// u / n_strips and strip u % n_strips, stepped without a division per tile.
+struct TileWalk {
+    int u, rt, st;
+    __device__ __forceinline__ explicit TileWalk(const DrArgs &p)
+        : u((int)blockIdx.x), rt((int)blockIdx.x / p.n_strips), st((int)blockIdx.x % p.n_strips)
+    {
+    }
+    __device__ __forceinline__ void next(const DrArgs &p)
+    {
+        u += (int)gridDim.x;
+        rt += p.grid_q;
+        st += p.grid_r;
+        if (st >= p.n_strips) {
+            st -= p.n_strips;
+            ++rt;
+        }
+    }
+};
 
 // The tile this CTA takes it-th; false past the CTA's share.
 __device__ __forceinline__ bool tile_of(const DrArgs &p, int n_units, int it, int &rt, int &st)
@@ -384,13 +405,13 @@ __device__ __forceinline__ void rht_pair(const uint32_t (&cw)[16], const uint2 (
 
 // The Philox outputs of columns h and h + 1 of one 16-row block: counters
 // n and n + nstep (n = (off_e H + h n_e + row) / 16, nstep = n_e / 16).  The
-// counter's second word, n / 2^32, is 0: the call's element positions are
-// below R_cap * H < 2^36 (the boundary refuses larger buffers).
-__device__ __forceinline__ void pair_random(const PhiloxKey &K, uint64_t n, uint32_t nstep, Philox4 &ra, Philox4 &rb)
+// call's element positions are below R_cap * H <= 2^36 (the boundary refuses
+// larger buffers), so every counter of the call fits the first word (32-bit
+// arithmetic is exact) and the counter's second word, n / 2^32, is 0.
+__device__ __forceinline__ void pair_random(const PhiloxKey &K, uint32_t n, uint32_t nstep, Philox4 &ra, Philox4 &rb)
 {
-    const uint64_t n1 = n + nstep;
-    ra = philox4x32_10((uint32_t)n, 0u, 1u, 0u, K);
-    rb = philox4x32_10((uint32_t)n1, 0u, 1u, 0u, K);
+    ra = philox4x32_10(n, 0u, 1u, 0u, K);
+    rb = philox4x32_10(n + nstep, 0u, 1u, 0u, K);
 }
 
 // The thread's four column pairs (8 columns x 16 rows).  With stochastic
@@ -398,25 +419,25 @@ __device__ __forceinline__ void pair_random(const PhiloxKey &K, uint64_t n, uint
 // current pair's arithmetic (independent work for the scheduler).
 template <bool kSR, bool kF16>
 __device__ __forceinline__ void rht_thread(const uint32_t (&cw)[16], const uint2 (&t16)[8], const float (&t32)[16],
-                                           const float *rcp, float se, float ce, const PhiloxKey &K, uint64_t nbase,
+                                           const float *rcp, float se, float ce, const PhiloxKey &K, uint32_t nbase,
                                            uint32_t nstep, uint8_t *outc, uint8_t *outs, int lane)
 {
     Philox4 ra, rb, na, nb;
     if (kSR)
         pair_random(K, nbase, nstep, ra, rb);
     if (kSR)
-        pair_random(K, nbase + 2 * (uint64_t)nstep, nstep, na, nb);
+        pair_random(K, nbase + 2 * nstep, nstep, na, nb);
     rht_pair<kSR, kF16, 0>(cw, t16, t32, rcp, se, ce, ra, rb, outc, outs, lane);
     if (kSR) {
         ra = na;
         rb = nb;
-        pair_random(K, nbase + 4 * (uint64_t)nstep, nstep, na, nb);
+        pair_random(K, nbase + 4 * nstep, nstep, na, nb);
     }
     rht_pair<kSR, kF16, 1>(cw, t16, t32, rcp, se, ce, ra, rb, outc, outs, lane);
     if (kSR) {
         ra = na;
         rb = nb;
-        pair_random(K, nbase + 6 * (uint64_t)nstep, nstep, na, nb);
+        pair_random(K, nbase + 6 * nstep, nstep, na, nb);
     }
     rht_pair<kSR, kF16, 2>(cw, t16, t32, rcp, se, ce, ra, rb, outc, outs, lane);
     rht_pair<kSR, kF16, 3>(cw, t16, t32, rcp, se, ce, na, nb, outc, outs, lane);
@@ -426,7 +447,7 @@ __device__ __forceinline__ void rht_thread(const uint32_t (&cw)[16], const uint2
 // the f16 decode scales): rare, kept out of line.
 template <bool kSR>
 __device__ __noinline__ void rht_thread_f32(const uint32_t (&cw)[16], const float (&t32)[16], const float *rcp,
-                                            float se, float ce, const PhiloxKey &K, uint64_t nbase, uint32_t nstep,
+                                            float se, float ce, const PhiloxKey &K, uint32_t nbase, uint32_t nstep,
                                             uint8_t *outc, uint8_t *outs, int lane)
 {
     const uint2 t16[8] = {};
@@ -520,8 +541,9 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
     int done = 0;
     bool ok = true;
     int prev_off = 0, prev_n = 0, prev_rl = 0, prev_st = 0;   // the tile before, staged, not yet stored
-    int rt, st;
-    for (int it = 0; tile_of(p, n_units, it, rt, st); ++it) {
+    int it = 0;
+    for (TileWalk tw(p); tw.u < n_units; tw.next(p), ++it) {
+        const int rt = tw.rt, st = tw.st;
         const int s = it % Sm::kNS;
         const uint32_t ph = (uint32_t)(it / Sm::kNS) & 1u;
         if (!mbar_wait_bounded(&sm.full[s], ph) || sm.abort_flag) {
@@ -639,10 +661,11 @@ __device__ __forceinline__ int consumer_loop(Sm &sm, const CUtensorMap *tm_rw, c
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 cw[i] = *reinterpret_cast<const uint32_t *>(&sm.codes[s][16 * warp + i][4 * lane]);
-            // Philox counter of column h0, this row block: (off_e H + h0 n_e + row) / 16
+            // Philox counter of column h0, this row block: (off_e H + h0 n_e + row) / 16,
+            // with off_e, n_e and the row multiples of 16 and the whole below 2^32
             const uint32_t nstep = (uint32_t)(m.n >> 4);
-            const uint64_t nbase = kSR ? ((uint64_t)m.off * (uint64_t)H + (uint64_t)h0 * (uint64_t)m.n +
-                                          (uint64_t)(rl + 16 * warp)) >> 4
+            const uint32_t nbase = kSR ? (uint32_t)(m.off >> 4) * (uint32_t)H + (uint32_t)h0 * nstep +
+                                             (uint32_t)((rl + 16 * warp) >> 4)
                                        : 0u;
             float t32[16];
             if (f16) {
@@ -956,6 +979,8 @@ cudaError_t launch_direct_receive(const LaunchCtx &c, const uint8_t *rows, int R
         grid = max_units;
     if (grid < 1)
         grid = 1;
+    a.grid_q = (int)grid / a.n_strips;
+    a.grid_r = (int)grid % a.n_strips;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, c.stream, tm_codes, tm_scales, tm_trailer,
                       tm_rw, tm_rws, a);
 }
