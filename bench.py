@@ -282,11 +282,11 @@ class BufferSet:
 
 
 def step_streams(set_bytes: int) -> int:
-    """Streams that take alternate steps: three for batches whose buffer set
+    """Streams that take alternate steps: four for batches whose buffer set
     holds less than 1 GB (their steps are short against the kernels' start-up
     and tail), two for larger ones (a third stream measured no faster on the
     16384-token, 256-expert batch and slower on the 64-expert one)."""
-    return 3 if set_bytes < (1 << 30) else 2
+    return 4 if set_bytes < (1 << 30) else 2
 
 
 def capture_rotation(torch, sets, rotations: int = 1, streams: int = 2):

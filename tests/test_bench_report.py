@@ -72,9 +72,9 @@ def test_traffic_comes_only_from_a_record_of_the_current_sources(tmp_path):
 
 
 def test_step_streams_and_set_rounding():
-    """Small batches take three streams, large ones two, and the rotating
+    """Small batches take four streams, large ones two, and the rotating
     sets are a multiple of the stream count, so a set stays on one stream."""
-    assert bench.step_streams(128 << 20) == 3 and bench.step_streams(900 << 20) == 3
+    assert bench.step_streams(128 << 20) == 4 and bench.step_streams(900 << 20) == 4
     assert bench.step_streams(1 << 30) == 2 and bench.step_streams(3 << 30) == 2
     for set_bytes in (64 << 20, 128 << 20, 700 << 20, 2 << 30, 3 << 30):
         ns = bench.step_streams(set_bytes)
