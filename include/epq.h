@@ -130,7 +130,7 @@ ep_status ep_route_plan(const int32_t *topk_idx, int64_t T, int k, int E, int A,
  *   Arguments, outputs and device status: as ep_route_plan.  Results are
  *   identical to ep_route_plan's for the same inputs.
  *   Limit: ep_route_workspace_bytes(T, k, E) must not exceed
- *   EP_ROUTE_STATIC_SCRATCH_BYTES (256 KiB: e.g. T <= 131072 tokens at
+ *   EP_ROUTE_STATIC_SCRATCH_BYTES (256 KiB: e.g. T <= 130560 tokens at
  *   E = 256); larger problems return EP_ERR_CAPACITY and launch nothing.
  *   Memory: allocates nothing, on any call.  The scratch is a fixed device
  *   array of EP_ROUTE_STATIC_SCRATCH_BYTES that every GPU which loads the

@@ -42,6 +42,9 @@ def test_size_helpers():
     assert L.ep_rows_capacity(4096, 2, 16, 128) == 4096 * 2 + 16 * 127
     assert L.ep_route_workspace_bytes(0, 2, 16) >= 16
     assert L.ep_route_workspace_bytes(16384, 8, 256) == 16 + 32 * 256 * 4
+    # the largest batch the fixed scratch of ep_route_plan_noalloc holds at E = 256
+    assert L.ep_route_workspace_bytes(130560, 8, 256) <= _lib.EP_ROUTE_STATIC_SCRATCH_BYTES
+    assert L.ep_route_workspace_bytes(130561, 8, 256) > _lib.EP_ROUTE_STATIC_SCRATCH_BYTES
 
 
 def test_status_strings():
