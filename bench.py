@@ -732,20 +732,34 @@ def oracle_pass(o, w, tokens, topk):
     o.nvfp4_direct_receive(rows, w.H, off, w.E, rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask)
 
 
-def oracle_expert_pass(o, w, experts) -> int:
+def oracle_expert_pass(o, w, experts, times: dict | None = None, other_ops: bool = False) -> int:
     """The batch's route plan + pack + direct receive on the oracle,
     restricted to the experts in ``experts``: every routing slot to another
     expert is dropped, so each kept expert has exactly its rows (and padding)
     of the whole batch, the pack writes only those rows and the receive
     builds only those experts' operands.  Returns the number of routed slots
-    kept; slots / k is the batch's work in tokens that the pass did."""
+    kept; slots / k is the batch's work in tokens that the pass did.
+    ``times`` (if given) receives the seconds of each call; with
+    ``other_ops`` the unpack of the packed rows and the MXFP8 pack of the same
+    slots follow (timed, outside the three calls of the path)."""
     topk = np.array(w.topk, copy=True)
     topk[~np.isin(topk, np.asarray(list(experts), dtype=np.int32))] = -1
+    t0 = time.perf_counter()
     off, cnt, dest, _ = o.route_plan(topk, w.E, w.A)
+    t1 = time.perf_counter()
     R_cap = int(off[-1])
     rows = o.nvfp4_pack(w.tokens, dest, w.k, off, cnt, w.E, max(R_cap, 1), rounding=w.rounding, seed=w.seed)
+    t2 = time.perf_counter()
     o.nvfp4_direct_receive(rows, w.H, off, w.E, rounding=w.rounding, seed=w.seed, sign_mask=w.sign_mask,
                            experts=list(experts))
+    t3 = time.perf_counter()
+    if times is not None:
+        times.update(route_plan=t1 - t0, pack=t2 - t1, direct_receive=t3 - t2)
+        if other_ops:
+            o.nvfp4_unpack(rows, w.H, off, w.E)
+            t4 = time.perf_counter()
+            o.mxfp8_pack(w.tokens, dest, w.k, off, cnt, w.E, max(R_cap, 1))
+            times.update(unpack=t4 - t3, mxfp8_pack=time.perf_counter() - t4)
     return int(np.count_nonzero(topk >= 0))
 
 
@@ -835,15 +849,18 @@ def cpu_baseline(w, cfg: int, budget_s: float = 10.0, all_cores: bool = True, kw
         acc += loads[m][1]
         m += 1
     experts = [e for e, _ in loads[:m]]
-    t0 = time.perf_counter()
-    slots = oracle_expert_pass(o, w, experts)
-    dt = time.perf_counter() - t0
+    times = {}
+    slots = oracle_expert_pass(o, w, experts, times, other_ops=True)
+    dt = times["route_plan"] + times["pack"] + times["direct_receive"]
     hc = host_cpu()
     res = {"value": slots / w.k / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "host_cpu": hc["model"],
            "nproc": hc["nproc"],
            "sample": f"route plan + pack + direct receive of {m} of the batch's {len(loads)} routed experts "
                      f"({slots} of {int(np.count_nonzero(w.topk >= 0))} slots, each expert with its rows and "
-                     f"padding of the whole batch), single-threaded C oracle, {dt:.2f} s; tokens = slots / k"}
+                     f"padding of the whole batch), single-threaded C oracle, {dt:.2f} s; tokens = slots / k",
+           "per_call": {"unit": UNIT, "sample": "the same slots, each call timed alone (the unpack decodes the "
+                                                "packed rows, the MXFP8 pack encodes the same slots)",
+                        **{op: slots / w.k / sec for op, sec in times.items()}}}
     if all_cores and hc["nproc"] > 1:
         import multiprocessing as mp
         C = hc["nproc"]

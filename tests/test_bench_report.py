@@ -13,6 +13,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 import bench  # noqa: E402
+import workloads  # noqa: E402
 
 
 def record(T=16384, H=7168, k=8, E=256, R=147200, ms_step=0.75, ms_a=0.15, ms_b=0.61):
@@ -86,3 +87,19 @@ def test_step_streams_and_set_rounding():
         for j in range(5 * n):
             owners.setdefault(j % n, set()).add(j % ns)
         assert all(len(v) == 1 for v in owners.values())
+
+
+def test_cpu_baseline_reports_each_call():
+    """The oracle's CPU baseline gives the path's rate and each call's alone
+    (route plan, pack, direct receive, and the unpack and MXFP8 pack of the
+    same slots), with the host's CPU named; the path's rate is that of the
+    three calls of the path together."""
+    w = workloads.make(1)
+    r = bench.cpu_baseline(w, 1, budget_s=0.5, all_cores=False)
+    assert r["kind"] == "oracle" and r["cores"] == 1 and r["host_cpu"] and r["nproc"] >= 1
+    pc = r["per_call"]
+    for op in ("route_plan", "pack", "direct_receive", "unpack", "mxfp8_pack"):
+        assert pc[op] > 0, op
+    # 1 / rate adds up over the calls of the path
+    inv = 1 / pc["route_plan"] + 1 / pc["pack"] + 1 / pc["direct_receive"]
+    assert abs(1 / inv - r["value"]) <= 1e-6 * r["value"]
