@@ -23,6 +23,10 @@ CASES = {
     "cfg5": dict(cfg=5, kw=dict(T=400, H=1024), unpack=False, mxfp8=True),
     "cfg1_ragged_H": dict(cfg=1, kw=dict(T=130, H=1056), unpack=True, mxfp8=True),
     "cfg4_ragged_H": dict(cfg=4, kw=dict(T=90, H=288, E=16, k=4), unpack=True, mxfp8=True),
+    # more tiles than the receive has CTAs, with a strip count (6) that does not
+    # divide the grid: every CTA steps to its later tiles across strip rows
+    "cfg3_tile_walk": dict(cfg=3, kw=dict(T=4000, H=1312), unpack=False),
+    "cfg4_tile_walk": dict(cfg=4, kw=dict(T=1200, H=1312, E=32, k=8), unpack=False),
 }
 
 
