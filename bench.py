@@ -241,6 +241,45 @@ def algorithmic_bytes(T, H, k, E, R, S):
     return route, pack, dr
 
 
+def row_bytes(H: int) -> int:
+    """Bytes of a packed NVFP4 row: roundup16(9H/16 + 16) (the boundary's
+    ep_nvfp4_row_bytes, restated for host arithmetic)."""
+    return (9 * H // 16 + 16 + 15) // 16 * 16
+
+
+def rows_capacity(T: int, k: int, E: int, A: int) -> int:
+    """Upper bound on the received rows of any routing, T k + E (A - 1) (the
+    boundary's ep_rows_capacity, restated for host arithmetic)."""
+    return T * k + E * (A - 1)
+
+
+def step_layout(w, n_sets: int = 0) -> dict:
+    """Buffer sets and step streams of the GPU arm's timed steps on workload
+    ``w`` (host arithmetic only): the bytes one set holds, the number of
+    rotating sets (a multiple of the streams) and the streams."""
+    T, H, k, E = w.T, w.H, w.k, w.E
+    R_cap = rows_capacity(T, k, E, w.A)
+    S = row_bytes(H)
+    set_bytes = 2 * T * H + 4 * T * k + R_cap * S * 2 + R_cap * (9 * H // 8 + 4)
+    nset = n_rotating_sets(set_bytes, n_sets)
+    ns = step_streams(set_bytes)
+    nset += (-nset) % ns   # every stream keeps its own sets
+    return dict(set_bytes=set_bytes, nset=nset, streams=ns, R_cap=R_cap, S=S)
+
+
+def workload_config(w, R: int, world: int, n_sets: int = 0) -> dict:
+    """The JSON ``config`` of a timed workload (both arms print the same):
+    the batch, its received rows R and the timing method of the GPU arm."""
+    lay = step_layout(w, n_sets)
+    set_mb = sum(algorithmic_bytes(w.T, w.H, w.k, w.E, R, lay["S"])) / 1e6
+    return {"workload": w.description, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "A": w.A, "R": R,
+            "rounding": "sr" if w.rounding else "rne",
+            "l2": f"{lay['nset']} rotating buffer sets ({set_mb:.0f} MB touched per step; a set is reused "
+                  f"after the others moved {(lay['nset'] - 1) * set_mb:.0f} MB through the 129 MB L2), "
+                  f"CUDA-graph steps, {lay['streams']} streams taking alternate steps",
+            "parallelism": f"replicas x{world}"}
+
+
 class BufferSet:
     """One set of device buffers and the CUDA graphs of one step on them."""
 
@@ -331,12 +370,9 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
     T, H, k, E = w.T, w.H, w.k, w.E
     tok_host = torch.from_numpy(w.tokens.view(np.int16)).view(torch.bfloat16)
     topk_host = torch.from_numpy(np.ascontiguousarray(w.topk))
-    S = nq.row_bytes(H)
-    R_cap = nq.rows_capacity(T, k, E, w.A)
-    set_bytes = 2 * T * H + 4 * T * k + R_cap * S * 2 + R_cap * (9 * H // 8 + 4)
-    nset = n_rotating_sets(set_bytes, n_sets)
-    ns = step_streams(set_bytes)
-    nset += (-nset) % ns   # every stream keeps its own sets
+    lay = step_layout(w, n_sets)
+    S, nset, ns = lay["S"], lay["nset"], lay["streams"]
+    assert S == nq.row_bytes(H) and lay["R_cap"] == nq.rows_capacity(T, k, E, w.A)
     sets = [BufferSet(torch, nq, w, tok_host, topk_host) for _ in range(nset)]
     torch.cuda.synchronize()
     st = int(sets[0].plan.status.item())
@@ -419,7 +455,8 @@ def time_steps(torch, nq, w, K, W, n_sets, barrier=None, clocks_enabled=True, gp
     st = int(sets[0].plan.status.item())
     route_b, pack_b, dr_b = algorithmic_bytes(T, H, k, E, R, S)
     set_mb = (route_b + pack_b + dr_b) / 1e6
-    return dict(sets=sets, tok_host=tok_host, topk_host=topk_host, nset=nset, streams=ns, set_mb=set_mb, T=T, H=H,
+    return dict(sets=sets, tok_host=tok_host, topk_host=topk_host, nset=nset, streams=ns, set_mb=set_mb,
+                n_sets_req=n_sets, T=T, H=H,
                 k=k, E=E,
                 R=R, S=S, ms_total=ms_total, ms_step=ms_total / K, ms_a=ms_a, ms_b=ms_b, wall_s=wall1 - wall0,
                 clocks=clk, status=st, bytes=(route_b, pack_b, dr_b), w=w, n_calls_timed=call_rot * nset, K=K, W=W)
@@ -434,12 +471,8 @@ def step_report(r, peak, peak_kind, world=1, config=None, n_sets_note=True) -> d
     dr_gbs = dr_b / (r["ms_b"] * 1e-3) / 1e9
     pack_gbs = (route_b + pack_b) / (r["ms_a"] * 1e-3) / 1e9
     path_gbs = (route_b + pack_b + dr_b) / (r["ms_step"] * 1e-3) / 1e9
-    cfg = {"workload": w.description, "T": r["T"], "H": r["H"], "E": r["E"], "k": r["k"], "A": w.A, "R": r["R"],
-           "rounding": "sr" if w.rounding else "rne",
-           "l2": f"{r['nset']} rotating buffer sets ({r['set_mb']:.0f} MB touched per step; a set is reused "
-                 f"after the others moved {(r['nset'] - 1) * r['set_mb']:.0f} MB through the 129 MB L2), "
-                 f"CUDA-graph steps, {r.get('streams', 1)} streams taking alternate steps",
-           "parallelism": f"replicas x{world}"}
+    cfg = workload_config(w, r["R"], world, r["n_sets_req"])
+    assert str(r["nset"]) + " rotating" in cfg["l2"] and f"{r['streams']} streams" in cfg["l2"]
     return {
         "value": tokens_s, "unit": UNIT, "ms_per_step": r["ms_step"], "steps": r["K"], "warmup": r["W"],
         "config": cfg,
@@ -910,10 +943,13 @@ def reference_arm(args, rank, world):
     dt = time.perf_counter() - t0
     value = slots / w.k / dt
     hc = host_cpu()
+    R = int(o.route_plan(w.topk, w.E, w.A)[0][-1])
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": dt * 1e3 / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.description, "experts_per_step": m, "tokens_per_step": slots / w.k / max(K, 1)},
+            # the GPU arm's config of the same batch; what one step here covers is in "sample"
+            "config": workload_config(w, R, world, args.sets),
+            "sample": {"experts_per_step": m, "tokens_per_step": slots / w.k / max(K, 1)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "host_cpu": hc["model"],
                              "nproc": hc["nproc"],
                              "sample": f"per step the route plan + pack + direct receive of {m} of the batch's "

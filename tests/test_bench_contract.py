@@ -24,3 +24,12 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert "workload" in d["config"]
+    # the reference line carries the GPU arm's config of the same batch
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import workloads
+    w = workloads.make(1)
+    R = int(oracle.route_plan(w.topk, w.E, w.A)[0][-1])
+    assert d["config"] == bench.workload_config(w, R, 1)
+    assert d["config"]["R"] == R and d["config"]["T"] == w.T

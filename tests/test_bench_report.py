@@ -18,9 +18,9 @@ import workloads  # noqa: E402
 
 def record(T=16384, H=7168, k=8, E=256, R=147200, ms_step=0.75, ms_a=0.15, ms_b=0.61):
     S = (9 * H // 16 + 16 + 15) // 16 * 16
-    w = types.SimpleNamespace(description="synthetic", A=128, rounding=1)
-    return dict(w=w, T=T, H=H, k=k, E=E, R=R, S=S, nset=2, set_mb=2600.0, ms_step=ms_step, ms_a=ms_a, ms_b=ms_b,
-                K=100, W=10, clocks=None, status=0, n_calls_timed=20,
+    w = types.SimpleNamespace(description="synthetic", A=128, rounding=1, T=T, H=H, k=k, E=E)
+    return dict(w=w, T=T, H=H, k=k, E=E, R=R, S=S, nset=2, streams=2, n_sets_req=0, set_mb=2600.0, ms_step=ms_step,
+                ms_a=ms_a, ms_b=ms_b, K=100, W=10, clocks=None, status=0, n_calls_timed=20,
                 bytes=bench.algorithmic_bytes(T, H, k, E, R, S))
 
 
